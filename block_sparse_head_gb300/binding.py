@@ -1,0 +1,226 @@
+"""ctypes binding of libbsa (include/bsa.h): argument marshalling only.
+
+Every step of the forward runs inside the library's CUDA kernel; torch supplies device
+memory and streams.  Calls fail loudly (``BsaError``) when the library is missing or
+a call returns an error; there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+BSA_ORDER_GLOBAL = 0
+BSA_ORDER_GROUPED = 1
+_ORDERS = {"global": BSA_ORDER_GLOBAL, "grouped": BSA_ORDER_GROUPED,
+           BSA_ORDER_GLOBAL: BSA_ORDER_GLOBAL, BSA_ORDER_GROUPED: BSA_ORDER_GROUPED}
+
+BSA_ERR_DEVICE_TIMEOUT = -8
+
+# Every symbol declared in include/bsa.h.
+EXPORTED = (
+    "bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_upload", "bsa_lut_free",
+    "bsa_forward", "bsa_device_status", "bsa_set_wait_limit", "bsa_wait_selftest",
+    "bsa_status_string", "bsa_version",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class BsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        text = _lib.bsa_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {text} ({status})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libbsa.so")
+
+
+def load_library():
+    """Load libbsa.so (built by ``block_sparse_head_gb300.build``) and declare its ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m block_sparse_head_gb300.build` "
+                "(the CUDA path has no fallback)")
+        lib = ctypes.CDLL(path)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        ip = ctypes.POINTER(ctypes.c_int)
+        vp = ctypes.c_void_p
+        lib.bsa_build_lut.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(vp)]
+        lib.bsa_lut_info.argtypes = [vp, ip, ip, ip, ip, ip]
+        lib.bsa_lut_export.argtypes = [vp, vp, vp, vp]
+        lib.bsa_lut_upload.argtypes = [vp, vp]
+        lib.bsa_lut_free.argtypes = [vp]
+        lib.bsa_lut_free.restype = None
+        lib.bsa_forward.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                    ctypes.c_int, vp]
+        lib.bsa_device_status.argtypes = [vp, vp, i32p]
+        lib.bsa_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        lib.bsa_wait_selftest.argtypes = [ctypes.c_uint64, vp]
+        lib.bsa_status_string.argtypes = [ctypes.c_int]
+        lib.bsa_status_string.restype = ctypes.c_char_p
+        lib.bsa_version.argtypes = []
+        lib.bsa_version.restype = ctypes.c_char_p
+        for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_upload",
+                     "bsa_forward", "bsa_device_status", "bsa_set_wait_limit",
+                     "bsa_wait_selftest"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise BsaError(status, what)
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Lut:
+    """A built look-up table (CSR of active column blocks + work list)."""
+
+    def __init__(self, layout, batch: int, order="global"):
+        lib = load_library()
+        lay = layout.detach().cpu().numpy() if isinstance(layout, torch.Tensor) else np.asarray(layout)
+        if lay.ndim != 3 or lay.shape[1] != lay.shape[2]:
+            raise ValueError(f"layout must be [H, nb, nb], got {lay.shape}")
+        lay = np.ascontiguousarray(lay.astype(np.int32, copy=False))
+        self._lib = lib
+        self.handle = ctypes.c_void_p()
+        _check(lib.bsa_build_lut(lay.ctypes.data, lay.shape[0], lay.shape[1], int(batch),
+                                 _ORDERS[order], ctypes.byref(self.handle)), "bsa_build_lut")
+        H, nb, b, nnz, n = (ctypes.c_int() for _ in range(5))
+        _check(lib.bsa_lut_info(self.handle, *(ctypes.byref(x) for x in (H, nb, b, nnz, n))),
+               "bsa_lut_info")
+        self.H, self.nb, self.batch = H.value, nb.value, b.value
+        self.nnz_total, self.n_items = nnz.value, n.value
+        self.device = None
+
+    def export(self):
+        """(row_ptr [H*nb+1], col_idx [nnz], items [n_items, 4]) as int32 numpy arrays."""
+        rp = np.empty(self.H * self.nb + 1, np.int32)
+        ci = np.empty(max(self.nnz_total, 1), np.int32)
+        it = np.empty((self.n_items, 4), np.int32)
+        _check(self._lib.bsa_lut_export(self.handle, rp.ctypes.data, ci.ctypes.data, it.ctypes.data),
+               "bsa_lut_export")
+        return rp, ci[:self.nnz_total], it
+
+    def upload(self, stream=None):
+        _check(self._lib.bsa_lut_upload(self.handle, _stream_handle(stream)), "bsa_lut_upload")
+        self.device = torch.cuda.current_device()
+        return self
+
+    def set_wait_limit(self, ns: int):
+        _check(self._lib.bsa_set_wait_limit(self.handle, int(ns)), "bsa_set_wait_limit")
+
+    def device_status(self, stream=None) -> tuple[int, int]:
+        """(status, raw word) of the device status word; synchronizes the stream."""
+        word = ctypes.c_int32(0)
+        st = self._lib.bsa_device_status(self.handle, _stream_handle(stream), ctypes.byref(word))
+        return st, word.value
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            self._lib.bsa_lut_free(h)
+            self.handle = None
+
+
+def build_lut(layout, batch: int, order="global", upload: bool | None = None, stream=None) -> Lut:
+    """Build the LUT on the host; upload it to the current CUDA device when one exists
+    (or when ``upload`` is True)."""
+    lut = Lut(layout, batch, order)
+    if upload is None:
+        upload = torch.cuda.is_available()
+    if upload:
+        lut.upload(stream)
+    return lut
+
+
+def _check_qkv(t: torch.Tensor, name: str, shape) -> None:
+    if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: float,
+            block: int, causal_diag: bool, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, stream=None):
+    """Block-sparse attention forward.  q, k, v: bf16 [B, H, L, d] on the LUT's device.
+    Returns (out bf16 [B, H, L, d], lse fp32 [B, H, L])."""
+    lib = load_library()
+    B, H, L, d = q.shape
+    _check_qkv(q, "q", (B, H, L, d))
+    _check_qkv(k, "k", (B, H, L, d))
+    _check_qkv(v, "v", (B, H, L, d))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, L, device=q.device, dtype=torch.float32)
+    _check_qkv(out, "out", (B, H, L, d))
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, L) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, L] tensor")
+    _check(lib.bsa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), lut.handle, out.data_ptr(),
+                           lse.data_ptr(), B, H, L, d, float(scale), int(block), int(bool(causal_diag)),
+                           _stream_handle(stream)), "bsa_forward")
+    return out, lse
+
+
+def forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: float,
+                 block: int, causal_diag: bool, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, dev_bufs=None, stream=None):
+    """Forward from host (ideally pinned) tensors: copies q, k, v to the device, runs
+    ``forward`` and copies out / lse back into host tensors, all on one stream.
+
+    ``dev_bufs`` may hold preallocated device tensors (q, k, v, out, lse) to reuse."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if dev_bufs is None:
+        dev_bufs = (torch.empty_like(q, device=dev), torch.empty_like(k, device=dev),
+                    torch.empty_like(v, device=dev), torch.empty_like(q, device=dev),
+                    torch.empty(q.shape[:3], device=dev, dtype=torch.float32))
+    dq, dk, dv, do, dl = dev_bufs
+    s = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(s):
+        dq.copy_(q, non_blocking=True)
+        dk.copy_(k, non_blocking=True)
+        dv.copy_(v, non_blocking=True)
+        forward(dq, dk, dv, lut, scale, block, causal_diag, out=do, lse=dl, stream=s)
+        if out is None:
+            out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        if lse is None:
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
+        out.copy_(do, non_blocking=True)
+        lse.copy_(dl, non_blocking=True)
+    return out, lse
+
+
+def wait_selftest(limit_ns: int = 1_000_000, stream=None) -> int:
+    """Run the bounded-wait self-test kernel; returns its status (expected
+    BSA_ERR_DEVICE_TIMEOUT = -8)."""
+    lib = load_library()
+    return lib.bsa_wait_selftest(int(limit_ns), _stream_handle(stream))
+
+
+def version() -> str:
+    return load_library().bsa_version().decode()

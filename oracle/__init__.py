@@ -1,0 +1,15 @@
+"""fp64 CPU oracle (test infrastructure only; see ``bsa_oracle``)."""
+
+from .bsa_oracle import (  # noqa: F401
+    ORDER_GLOBAL,
+    ORDER_GROUPED,
+    active_keys,
+    block_flops,
+    check_layout,
+    expand_mask,
+    forward,
+    forward_dense,
+    masked_attention,
+    oracle_lut,
+    query_block,
+)

@@ -1,0 +1,449 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each check below would fail for a plausible slip in the oracle: dropping the -inf
+masking (multiplying scores by the mask instead), flipping the causal comparison,
+transposing Q K^T, forgetting the max term of the log-sum-exp, leaving masked keys
+in the softmax denominator, or mis-ordering the CSR / work list.  The last tests
+plant such slips in copies of the oracle and check that the pins catch them.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import bsa_oracle as ob
+from block_sparse_head_gb300 import workloads as wls
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _sdpa(q, k, v, scale, is_causal=False):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))  # noqa: E731
+    o = F.scaled_dot_product_attention(t(q), t(k), t(v), scale=scale, is_causal=is_causal)
+    return o.numpy()
+
+
+def _lse_ref(q, k, scale, causal=False):
+    s = torch.from_numpy(scale * np.einsum("bhqd,bhkd->bhqk", q, k))
+    if causal:
+        L = s.shape[-1]
+        s = s.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+    return torch.logsumexp(s, dim=-1).numpy()
+
+
+# ------------------------------------------------------- reductions to library routines
+
+
+def pin_dense(fwd):
+    """All-ones layout == textbook dense attention ("Scaled Dot-Product Attention")."""
+    B, H, nb, blk, d = 2, 2, 4, 8, 16
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (1, 2, 3))
+    lay = np.ones((H, nb, nb), np.int32)
+    scale = 0.37
+    o, lse = fwd(q, k, v, lay, scale, blk, False)
+    return max(np.abs(o - _sdpa(q, k, v, scale)).max(), np.abs(lse - _lse_ref(q, k, scale)).max())
+
+
+def pin_causal(fwd):
+    """Lower-triangular layout + causal diagonal == causal dense attention."""
+    B, H, nb, blk, d = 1, 3, 5, 4, 8
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (4, 5, 6))
+    lay = np.tril(np.ones((nb, nb), np.int32))[None].repeat(H, 0)
+    scale = 1 / math.sqrt(d)
+    o, lse = fwd(q, k, v, lay, scale, blk, True)
+    ref = _sdpa(q, k, v, scale, is_causal=True)
+    return max(np.abs(o - ref).max(), np.abs(lse - _lse_ref(q, k, scale, causal=True)).max())
+
+
+def pin_block_diagonal(fwd):
+    """eye(nb) layout == independent dense attention inside each block
+    ("Block Sparse Attention Techniques" 3.2, block-diagonal patterns; the
+    "diagonal" pattern of the "Block-Sparse Attention" page)."""
+    B, H, nb, blk, d = 2, 1, 4, 8, 8
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (7, 8, 9))
+    lay = np.eye(nb, dtype=np.int32)[None]
+    scale = 0.5
+    o, _ = fwd(q, k, v, lay, scale, blk, False)
+    err = 0.0
+    for i in range(nb):
+        sl = slice(i * blk, (i + 1) * blk)
+        ref = _sdpa(q[:, :, sl], k[:, :, sl], v[:, :, sl], scale)
+        err = max(err, np.abs(o[:, :, sl] - ref).max())
+    return err
+
+
+def brute_force(q, k, v, lay, scale, blk, causal):
+    """Per-element triple loops in plain Python floats (tiny inputs only)."""
+    B, H, L, d = q.shape
+    o = np.zeros((B, H, L, d))
+    lse = np.full((B, H, L), -math.inf)
+    for b in range(B):
+        for h in range(H):
+            for r in range(L):
+                keys = []
+                for c in range(L):
+                    if lay[h][r // blk][c // blk] != 1:
+                        continue
+                    if causal and r // blk == c // blk and c > r:
+                        continue
+                    keys.append(c)
+                if not keys:
+                    continue
+                sc = {}
+                for c in keys:
+                    acc = 0.0
+                    for x in range(d):
+                        acc += float(q[b, h, r, x]) * float(k[b, h, c, x])
+                    sc[c] = scale * acc
+                mx = max(sc.values())
+                tot = sum(math.exp(sc[c] - mx) for c in keys)
+                lse[b, h, r] = mx + math.log(tot)
+                for x in range(d):
+                    o[b, h, r, x] = sum(math.exp(sc[c] - mx) / tot * float(v[b, h, c, x]) for c in keys)
+    return o, lse
+
+
+def pin_brute(fwd, seed=11, causal=True):
+    B, H, nb, blk, d = 2, 2, 4, 4, 3
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), seed + s) for s in range(3))
+    rng = np.random.default_rng(seed)
+    lay = (rng.random((H, nb, nb)) < 0.5).astype(np.int32)
+    lay[0, 1] = 0  # an empty row
+    lay[1, 2] = 1  # a full row
+    o, lse = fwd(q, k, v, lay, 0.8, blk, causal)
+    ro, rl = brute_force(q, k, v, lay, 0.8, blk, causal)
+    fin = np.isfinite(rl)
+    if not np.array_equal(fin, np.isfinite(lse)):
+        return math.inf
+    return max(np.abs(o - ro).max(), np.abs(lse[fin] - rl[fin]).max() if fin.any() else 0.0)
+
+
+FWDS = [("forward", oracle.forward), ("forward_dense", oracle.forward_dense)]
+
+
+@pytest.mark.parametrize("name,fwd", FWDS)
+def test_dense_layout_is_sdpa(name, fwd):
+    assert pin_dense(fwd) < 1e-12
+
+
+@pytest.mark.parametrize("name,fwd", FWDS)
+def test_causal_layout_is_causal_sdpa(name, fwd):
+    assert pin_causal(fwd) < 1e-12
+
+
+@pytest.mark.parametrize("name,fwd", FWDS)
+def test_block_diagonal_is_per_block_sdpa(name, fwd):
+    assert pin_block_diagonal(fwd) < 1e-12
+
+
+@pytest.mark.parametrize("name,fwd", FWDS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_tiny(name, fwd, causal):
+    assert pin_brute(fwd, causal=causal) < 1e-12
+
+
+def test_skip_equals_dense_mask():
+    """Skipping keys outside active blocks (query-block path) equals the full [L, L]
+    masked softmax, on random layouts with empty rows, both causal settings."""
+    for seed, causal in [(21, False), (22, True), (23, True)]:
+        B, H, nb, blk, d = 2, 3, 6, 8, 16
+        L = nb * blk
+        q, k, v = (_rand((B, H, L, d), seed * 10 + s) for s in range(3))
+        lay = wls.random_layout(H, nb, 0.35, seed, empty_rows=1).numpy()
+        o1, l1 = oracle.forward(q, k, v, lay, 0.3, blk, causal)
+        o2, l2 = oracle.forward_dense(q, k, v, lay, 0.3, blk, causal)
+        assert np.array_equal(np.isfinite(l1), np.isfinite(l2))
+        assert np.abs(o1 - o2).max() < 1e-12
+        fin = np.isfinite(l1)
+        assert np.abs(l1[fin] - l2[fin]).max() < 1e-12
+
+
+# --------------------------------------------------------------------- closed forms
+
+
+def test_golden_hand_example():
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "hand_example.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    q = np.ones((1, 2, 4, 1))
+    k = np.array([0.0, math.log(3), 0.0, math.log(2)]).reshape(1, 1, 4, 1).repeat(2, 1)
+    v = np.array([1.0, 2.0, 4.0, 8.0]).reshape(1, 1, 4, 1).repeat(2, 1)
+    lay = np.array([[[1, 0], [1, 1]], [[0, 0], [1, 1]]], np.int32)
+    for fwd in (oracle.forward, oracle.forward_dense):
+        o, lse = fwd(q, k, v, lay, 1.0, 2, True)
+        for h, r, num, den, arg in (map(int, x) for x in rows):
+            assert abs(o[0, h, r, 0] - num / den) < 1e-12
+            want = math.log(arg) if arg else -math.inf
+            assert lse[0, h, r] == want or abs(lse[0, h, r] - want) < 1e-12
+
+
+def test_scale_zero_is_mean_of_active_rows():
+    B, H, nb, blk, d = 1, 2, 5, 4, 6
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (31, 32, 33))
+    lay = wls.random_layout(H, nb, 0.4, 3, empty_rows=1).numpy()
+    o, lse = oracle.forward(q, k, v, lay, 0.0, blk, True)
+    for h in range(H):
+        for r in range(L):
+            a = oracle.active_keys(lay[h], blk, True, r)
+            if a.size == 0:
+                assert np.all(o[0, h, r] == 0) and lse[0, h, r] == -math.inf
+            else:
+                assert np.abs(o[0, h, r] - v[0, h, a].mean(0)).max() < 1e-12
+                assert abs(lse[0, h, r] - math.log(a.size)) < 1e-12
+
+
+def test_constant_v_and_zero_k():
+    B, H, nb, blk, d = 1, 1, 4, 8, 4
+    L = nb * blk
+    q, k, _ = (_rand((B, H, L, d), s) for s in (41, 42, 43))
+    lay = np.tril(np.ones((nb, nb), np.int32))[None]
+    v = np.full((B, H, L, d), 2.5)
+    o, _ = oracle.forward(q, k, v, lay, 0.7, blk, True)
+    assert np.abs(o - 2.5).max() < 1e-12
+    v2 = _rand((B, H, L, d), 44)
+    o2, lse2 = oracle.forward(q, np.zeros_like(k), v2, lay, 0.7, blk, True)
+    for r in range(L):
+        a = oracle.active_keys(lay[0], blk, True, r)
+        assert np.abs(o2[0, 0, r] - v2[0, 0, a].mean(0)).max() < 1e-12
+        assert abs(lse2[0, 0, r] - math.log(a.size)) < 1e-12
+
+
+# ----------------------------------------------------------------------- invariants
+
+
+def test_invariants_probabilities_hull_empty_rows():
+    B, H, nb, blk, d = 2, 2, 6, 8, 8
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (51, 52, 53))
+    lay = wls.random_layout(H, nb, 0.3, 5, empty_rows=2).numpy()
+    scale = 0.6
+    o, lse = oracle.forward(q, k, v, lay, scale, blk, True)
+    for b in range(B):
+        for h in range(H):
+            for r in range(L):
+                a = oracle.active_keys(lay[h], blk, True, r)
+                if a.size == 0:
+                    assert np.all(o[b, h, r] == 0) and lse[b, h, r] == -math.inf
+                    continue
+                p = np.exp(scale * (k[b, h, a] @ q[b, h, r]) - lse[b, h, r])
+                assert abs(p.sum() - 1) < 1e-12
+                lo, hi = v[b, h, a].min(0), v[b, h, a].max(0)
+                assert np.all(o[b, h, r] >= lo - 1e-12) and np.all(o[b, h, r] <= hi + 1e-12)
+
+
+def test_invariant_row_permutation_inside_block():
+    """Permuting key rows inside a key block (K and V jointly) changes nothing for the
+    query rows that see that block unmasked (all rows without a causal diagonal;
+    rows of other query blocks with it)."""
+    B, H, nb, blk, d = 1, 1, 4, 8, 8
+    L = nb * blk
+    q, k, v = (_rand((B, H, L, d), s) for s in (61, 62, 63))
+    lay = np.tril(np.ones((nb, nb), np.int32))[None]
+    perm = np.arange(L)
+    perm[0:blk] = np.random.default_rng(0).permutation(blk)
+    for causal, rows in ((False, slice(0, L)), (True, slice(blk, L))):
+        o, lse = oracle.forward(q, k, v, lay, 0.5, blk, causal)
+        o2, lse2 = oracle.forward(q, k[:, :, perm], v[:, :, perm], lay, 0.5, blk, causal)
+        assert np.abs(o[:, :, rows] - o2[:, :, rows]).max() < 1e-12
+        assert np.abs(lse[:, :, rows] - lse2[:, :, rows]).max() < 1e-12
+
+
+# ---------------------------------------------------------------------- mask expansion
+
+
+def test_expand_mask_matches_page_patterns():
+    """The "diagonal" and "tridiagonal" patterns of the "Block-Sparse Attention" page
+    (seq_len 32, block_size 4), built independently with a Kronecker product."""
+    nb, blk, L = 8, 4, 32
+    diag = oracle.expand_mask(np.eye(nb, dtype=np.int32), blk, L, False)
+    assert np.array_equal(diag, np.kron(np.eye(nb), np.ones((blk, blk))).astype(bool))
+    tri_lay = (np.abs(np.subtract.outer(np.arange(nb), np.arange(nb))) <= 1).astype(np.int32)
+    tri = oracle.expand_mask(tri_lay, blk, L, False)
+    ii = np.arange(L) // blk
+    assert np.array_equal(tri, np.abs(ii[:, None] - ii[None, :]) <= 1)
+    causal = oracle.expand_mask(np.eye(nb, dtype=np.int32), blk, L, True)
+    r, c = np.meshgrid(np.arange(L), np.arange(L), indexing="ij")
+    assert np.array_equal(causal, (r // blk == c // blk) & (c <= r))
+
+
+def test_printed_pair_count():
+    """65,536 computed pairs printed by the "Block-Sparse Attention" page."""
+    kv = dict(ln.split() for ln in open(os.path.join(GOLDEN, "printed_pair_count.txt"))
+              if ln.strip() and not ln.startswith("#"))
+    n, b, k = int(kv["seq_len"]), int(kv["block"]), int(kv["blocks_per_row"])
+    nb = n // b
+    lay = np.zeros((1, nb, nb), np.int32)
+    for i in range(nb):
+        lay[0, i, i] = 1  # one active block per query block
+    d = 64
+    assert oracle.block_flops(lay, 1, b, d) // (4 * d) == int(kv["pairs"]) == n * k * b
+    assert int(oracle.expand_mask(lay[0], b, n, False).sum()) == int(kv["pairs"])
+
+
+# ------------------------------------------------------------------------------- LUT
+
+
+def _read_lut_golden():
+    rp = ci = None
+    items = []
+    for ln in open(os.path.join(GOLDEN, "lut_tiny_band1.txt")):
+        if not ln.strip() or ln.startswith("#"):
+            continue
+        tag, *vals = ln.split()
+        if tag == "row_ptr":
+            rp = [int(x) for x in vals]
+        elif tag == "col_idx":
+            ci = [int(x) for x in vals]
+        else:
+            items.append([int(x) for x in vals])
+    return rp, ci, items
+
+
+def test_lut_golden_tiny():
+    rp, ci, items = _read_lut_golden()
+    lay = wls.layout_for(wls.WORKLOADS[1]).numpy()
+    r, c, it = oracle.oracle_lut(lay, 1)
+    assert r.tolist() == rp and c.tolist() == ci and it.tolist() == items
+
+
+def _count_cfg5_row(i):
+    return min(i, 7) + 1 + sum(1 for j in range(0, i - 7) if j % 16 == 15)
+
+
+def test_lut_closed_form_counts():
+    # workload 2: band |i-j| <= 4 on 64 blocks -> 64*9 - 2*(4+3+2+1) = 556 per head,
+    # sparsity 1 - 556/4096 = 86.43% (the DeepSpeed utils page's bandwidth-4 example).
+    lay2 = wls.layout_for(wls.WORKLOADS[2]).numpy()
+    rp, ci, it = oracle.oracle_lut(lay2, 1)
+    assert rp[-1] == 8 * 556 and ci.size == 8 * 556
+    assert abs((lay2 == 0).mean() - 0.8643) < 5e-5
+    # workload 3: row i has min(i, 3) + 1 window blocks plus column 0 when i >= 4.
+    lay3 = wls.layout_for(wls.WORKLOADS[3]).numpy()
+    rp3, _, it3 = oracle.oracle_lut(lay3, 2)
+    counts = np.diff(rp3)[:64]
+    assert counts.tolist() == [min(i, 3) + 1 + (1 if i >= 4 else 0) for i in range(64)]
+    assert rp3[-1] == 16 * 310
+    assert it3.shape == (2 * 16 * 64, 4)
+    # workload 5: band of 8 plus the strided columns at or below the band's start.
+    lay5 = wls.layout_for(wls.WORKLOADS[5]).numpy()
+    rows5 = lay5[0].sum(1)
+    assert rows5.tolist() == [_count_cfg5_row(i) for i in range(512)]
+    assert int(rows5.sum()) == 11787
+
+
+def test_lut_structure_random():
+    for seed in range(4):
+        H, nb, B = 3, 7, 2
+        lay = wls.random_layout(H, nb, 0.4, seed, empty_rows=2).numpy()
+        for order in ("global", "grouped"):
+            rp, ci, it = oracle.oracle_lut(lay, B, order)
+            assert rp[0] == 0 and rp[-1] == lay.sum() == ci.size
+            for h in range(H):
+                for i in range(nb):
+                    row = ci[rp[h * nb + i]:rp[h * nb + i + 1]]
+                    assert row.tolist() == np.nonzero(lay[h, i])[0].tolist()
+            keys = {tuple(x[:3]) for x in it.tolist()}
+            assert len(keys) == B * H * nb  # a permutation of every (b, h, i)
+            for b_, h_, i_, n_ in it.tolist():
+                assert n_ == lay[h_, i_].sum()
+            if order == "global":
+                k = [(-x[3], x[0], x[1], x[2]) for x in it.tolist()]
+            else:
+                k = [(x[0], x[1], -x[3], x[2]) for x in it.tolist()]
+            assert k == sorted(k)
+
+
+def test_layout_validation():
+    with pytest.raises(ValueError):
+        oracle.oracle_lut(np.full((1, 2, 2), 2, np.int32), 1)
+    with pytest.raises(ValueError):
+        oracle.oracle_lut(np.ones((1, 2, 3), np.int32), 1)
+    with pytest.raises(ValueError):
+        oracle.oracle_lut(np.ones((1, 2, 2), np.int32), 0)
+
+
+def test_workload_layout_counts():
+    """Generator sanity for workload 4: per-head active counts stay near 10% of the
+    strict lower triangle plus the diagonal."""
+    lay4 = wls.layout_for(wls.WORKLOADS[4]).numpy()
+    per_head = lay4.reshape(16, -1).sum(1)
+    expect = 0.10 * 256 * 255 / 2 + 256
+    assert np.all(np.abs(per_head - expect) < 200)
+    assert np.all(np.triu(lay4[0], 1) == 0) and np.all(np.diagonal(lay4, axis1=1, axis2=2) == 1)
+
+
+# --------------------------------------------------------- planted mistakes are caught
+
+
+def _mutant_forward(masked_attention_impl=None, expand_impl=None):
+    def fwd(q, k, v, layout, scale, block, causal):
+        saved = (ob.masked_attention, ob.expand_mask)
+        try:
+            if masked_attention_impl is not None:
+                ob.masked_attention = masked_attention_impl
+            if expand_impl is not None:
+                ob.expand_mask = expand_impl
+            return ob.forward_dense(q, k, v, layout, scale, block, causal)
+        finally:
+            ob.masked_attention, ob.expand_mask = saved
+    return fwd
+
+
+def _multiply_mask(q, k, v, mask, scale):  # literal "softmax(S * M)": masked logit 0
+    s = scale * (q @ k.T) * mask
+    m = s.max(1, keepdims=True)
+    e = np.exp(s - m)
+    return (e / e.sum(1, keepdims=True)) @ v, (m + np.log(e.sum(1, keepdims=True)))[:, 0]
+
+
+def _no_max_in_lse(q, k, v, mask, scale):
+    o, lse = saved_masked(q, k, v, mask, scale)
+    s = np.where(mask, scale * (q @ k.T), -np.inf)
+    return o, np.where(np.isfinite(lse), lse - s.max(1), lse)
+
+
+def _transposed(q, k, v, mask, scale):
+    return saved_masked(k, q, v, mask, scale)
+
+
+def _flipped_causal(layout_h, block, L, causal_diag):
+    m = saved_expand(layout_h, block, L, False)
+    if causal_diag:
+        for i in range(L // block):
+            for rr in range(block):
+                r = i * block + rr
+                m[r, i * block:r] = False
+    return m
+
+
+saved_masked = ob.masked_attention
+saved_expand = ob.expand_mask
+
+
+@pytest.mark.parametrize("mutant", [
+    _mutant_forward(masked_attention_impl=_multiply_mask),
+    _mutant_forward(masked_attention_impl=_no_max_in_lse),
+    _mutant_forward(masked_attention_impl=_transposed),
+    _mutant_forward(expand_impl=_flipped_causal),
+])
+def test_pins_catch_planted_mistakes(mutant):
+    errs = []
+    for pin in (pin_dense, pin_causal, pin_block_diagonal, pin_brute):
+        try:
+            errs.append(pin(mutant))
+        except Exception:  # a shape error is a catch too
+            errs.append(math.inf)
+    assert max(errs) > 1e-6
