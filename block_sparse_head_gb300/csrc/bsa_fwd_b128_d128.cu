@@ -1,0 +1,11 @@
+// Forward kernel instance for block 128, head dim 128.
+#include "bsa_fwd_kernel.cuh"
+
+namespace bsa {
+
+cudaError_t launch_fwd_b128_d128(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, int grid, cudaStream_t stream) {
+  return launch_fwd<128, 128>(p, q, k, v, grid, stream);
+}
+
+}  // namespace bsa

@@ -1,0 +1,313 @@
+// bsa_host.cpp -- host side of libbsa: LUT construction (CSR + work list), argument
+// validation, TMA descriptor encoding and kernel launch.  See include/bsa.h for the
+// contract of every exported function.
+#include "../../include/bsa.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <new>
+
+#include <cudaTypedefs.h>
+
+#include "bsa_internal.h"
+
+namespace {
+
+constexpr int64_t kInt32Max = std::numeric_limits<int32_t>::max();
+
+// ------------------------------------------------------------- LUT building
+
+// Work-list keys.  Items are generated in (b, h, i) order, so a stable sort on the
+// remaining key fields yields the documented total orders.
+bool less_global(const int32_t* a, const int32_t* b) { return a[3] > b[3]; }
+
+bool less_grouped(const int32_t* a, const int32_t* b) {
+  if (a[0] != b[0]) return a[0] < b[0];
+  if (a[1] != b[1]) return a[1] < b[1];
+  return a[3] > b[3];
+}
+
+// ------------------------------------------------------------ TMA encoding
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows, d] bf16 view of a [B,H,L,d] tensor; box = 64 columns x `box_rows` rows,
+// 128-byte swizzle (matches the kernel's shared-memory operand layout).
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count(int dev) {
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_device(bsa_lut* lut) {
+  if (lut->d_row_ptr) cudaFree(lut->d_row_ptr);
+  if (lut->d_col_idx) cudaFree(lut->d_col_idx);
+  if (lut->d_items) cudaFree(lut->d_items);
+  if (lut->d_status) cudaFree(lut->d_status);
+  lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = nullptr;
+  lut->device = -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bsa_lut** out) {
+  if (out == nullptr) return BSA_ERR_NULL;
+  *out = nullptr;
+  if (layout == nullptr) return BSA_ERR_NULL;
+  if (H < 1 || nb < 1 || batch < 1) return BSA_ERR_SHAPE;
+  const int64_t cells = static_cast<int64_t>(H) * nb * nb;
+  const int64_t n_items = static_cast<int64_t>(batch) * H * nb;
+  if (cells > kInt32Max || n_items > kInt32Max) return BSA_ERR_SHAPE;
+  if (order != BSA_ORDER_GLOBAL && order != BSA_ORDER_GROUPED) return BSA_ERR_UNSUPPORTED;
+  for (int64_t e = 0; e < cells; ++e)
+    if (layout[e] != 0 && layout[e] != 1) return BSA_ERR_LAYOUT_VALUE;
+
+  bsa_lut* lut = new (std::nothrow) bsa_lut();
+  if (lut == nullptr) return BSA_ERR_ALLOC;
+  try {
+    lut->H = H;
+    lut->nb = nb;
+    lut->batch = batch;
+    lut->order = order;
+    const int rows = H * nb;
+    lut->row_ptr.assign(rows + 1, 0);
+    for (int r = 0; r < rows; ++r) {
+      const int32_t* lr = layout + static_cast<int64_t>(r) * nb;
+      int cnt = 0;
+      for (int j = 0; j < nb; ++j) cnt += lr[j];
+      lut->row_ptr[r + 1] = lut->row_ptr[r] + cnt;
+    }
+    lut->nnz_total = lut->row_ptr[rows];
+    lut->col_idx.resize(lut->nnz_total);
+    for (int r = 0; r < rows; ++r) {
+      const int32_t* lr = layout + static_cast<int64_t>(r) * nb;
+      int32_t* dst = lut->col_idx.data() + lut->row_ptr[r];
+      for (int j = 0; j < nb; ++j)
+        if (lr[j]) *dst++ = j;
+    }
+    lut->n_items = static_cast<int>(n_items);
+    std::vector<int32_t> raw(static_cast<size_t>(n_items) * 4);
+    size_t w = 0;
+    for (int b = 0; b < batch; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int i = 0; i < nb; ++i) {
+          const int r = h * nb + i;
+          raw[w++] = b;
+          raw[w++] = h;
+          raw[w++] = i;
+          raw[w++] = lut->row_ptr[r + 1] - lut->row_ptr[r];
+        }
+    std::vector<const int32_t*> idx(static_cast<size_t>(n_items));
+    for (size_t e = 0; e < idx.size(); ++e) idx[e] = raw.data() + 4 * e;
+    std::stable_sort(idx.begin(), idx.end(),
+                     order == BSA_ORDER_GLOBAL ? less_global : less_grouped);
+    lut->items.resize(raw.size());
+    for (size_t e = 0; e < idx.size(); ++e) std::memcpy(&lut->items[4 * e], idx[e], 16);
+  } catch (const std::bad_alloc&) {
+    delete lut;
+    return BSA_ERR_ALLOC;
+  }
+  *out = lut;
+  return BSA_OK;
+}
+
+int bsa_lut_info(const bsa_lut* lut, int* H, int* nb, int* batch, int* nnz_total, int* n_items) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (H) *H = lut->H;
+  if (nb) *nb = lut->nb;
+  if (batch) *batch = lut->batch;
+  if (nnz_total) *nnz_total = lut->nnz_total;
+  if (n_items) *n_items = lut->n_items;
+  return BSA_OK;
+}
+
+int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32_t* items) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (row_ptr) std::memcpy(row_ptr, lut->row_ptr.data(), lut->row_ptr.size() * 4);
+  if (col_idx && !lut->col_idx.empty())
+    std::memcpy(col_idx, lut->col_idx.data(), lut->col_idx.size() * 4);
+  if (items) std::memcpy(items, lut->items.data(), lut->items.size() * 4);
+  return BSA_OK;
+}
+
+int bsa_lut_upload(bsa_lut* lut, void* stream) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  free_device(lut);
+  const size_t nr = lut->row_ptr.size() * 4;
+  const size_t nc = std::max<size_t>(lut->col_idx.size(), 1) * 4;
+  const size_t ni = lut->items.size() * 4;
+  if (cudaMalloc(&lut->d_row_ptr, nr) != cudaSuccess || cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess ||
+      cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess) {
+    free_device(lut);
+    cudaGetLastError();
+    return BSA_ERR_ALLOC;
+  }
+  bool ok = cudaMemcpyAsync(lut->d_row_ptr, lut->row_ptr.data(), nr, cudaMemcpyHostToDevice, st) ==
+                cudaSuccess &&
+            (lut->col_idx.empty() ||
+             cudaMemcpyAsync(lut->d_col_idx, lut->col_idx.data(), lut->col_idx.size() * 4,
+                             cudaMemcpyHostToDevice, st) == cudaSuccess) &&
+            cudaMemcpyAsync(lut->d_items, lut->items.data(), ni, cudaMemcpyHostToDevice, st) ==
+                cudaSuccess &&
+            cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
+            cudaStreamSynchronize(st) == cudaSuccess;
+  if (!ok) {
+    free_device(lut);
+    return BSA_ERR_CUDA;
+  }
+  lut->device = dev;
+  return BSA_OK;
+}
+
+void bsa_lut_free(bsa_lut* lut) {
+  if (lut == nullptr) return;
+  free_device(lut);
+  delete lut;
+}
+
+int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
+                float* lse, int B, int H, int L, int d, float scale, int block, int causal_diag,
+                void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || lut == nullptr || out == nullptr ||
+      lse == nullptr)
+    return BSA_ERR_NULL;
+  if ((block != 64 && block != 128) || (d != 64 && d != 128)) return BSA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return BSA_ERR_UNSUPPORTED;
+  if (B != lut->batch || H != lut->H || L <= 0 || static_cast<int64_t>(lut->nb) * block != L)
+    return BSA_ERR_SHAPE;
+  const int64_t rows = static_cast<int64_t>(B) * H * L;
+  if (rows > kInt32Max) return BSA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return BSA_ERR_ALIGN;
+  if (lut->d_items == nullptr) return BSA_ERR_STATE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev != lut->device) return BSA_ERR_STATE;
+
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows(&tq, q, rows, d, block) || !encode_rows(&tk, k, rows, d, block) ||
+      !encode_rows(&tv, v, rows, d, block))
+    return BSA_ERR_CUDA;
+
+  bsa::FwdParams p{};
+  p.items = reinterpret_cast<const int4*>(lut->d_items);
+  p.row_ptr = lut->d_row_ptr;
+  p.col_idx = lut->d_col_idx;
+  p.out = out;
+  p.lse = lse;
+  p.status = lut->d_status;
+  p.n_items = lut->n_items;
+  p.H = H;
+  p.L = L;
+  p.nb = lut->nb;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.causal_diag = causal_diag != 0;
+  p.wait_limit_ns = lut->wait_limit_ns;
+
+  const int sms = sm_count(dev);
+  if (sms <= 0) return BSA_ERR_CUDA;
+  const int grid = std::max(1, std::min(lut->n_items, sms));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (block == 128 && d == 128)
+    e = bsa::launch_fwd_b128_d128(p, tq, tk, tv, grid, st);
+  else if (block == 128)
+    e = bsa::launch_fwd_b128_d64(p, tq, tk, tv, grid, st);
+  else if (d == 128)
+    e = bsa::launch_fwd_b64_d128(p, tq, tk, tv, grid, st);
+  else
+    e = bsa::launch_fwd_b64_d64(p, tq, tk, tv, grid, st);
+  return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+int bsa_device_status(const bsa_lut* lut, void* stream, int32_t* detail) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (lut->d_status == nullptr) return BSA_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpyAsync(&word, lut->d_status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(lut->d_status, 0, 4, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (detail) *detail = word;
+  return word == 0 ? BSA_OK : BSA_ERR_DEVICE_TIMEOUT;
+}
+
+int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  lut->wait_limit_ns = ns == 0 ? 10000000000ull : ns;
+  return BSA_OK;
+}
+
+int bsa_wait_selftest(uint64_t limit_ns, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* d = nullptr;
+  if (cudaMalloc(&d, 4) != cudaSuccess) return BSA_ERR_ALLOC;
+  int32_t word = 0;
+  bool ok = cudaMemsetAsync(d, 0, 4, st) == cudaSuccess &&
+            bsa::launch_wait_selftest(d, limit_ns, st) == cudaSuccess &&
+            cudaMemcpyAsync(&word, d, 4, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+            cudaStreamSynchronize(st) == cudaSuccess;
+  cudaFree(d);
+  if (!ok) return BSA_ERR_CUDA;
+  return word == (bsa::kSiteSelftest | 0x10000) ? BSA_ERR_DEVICE_TIMEOUT : BSA_OK;
+}
+
+const char* bsa_status_string(int status) {
+  switch (status) {
+    case BSA_OK: return "ok";
+    case BSA_ERR_NULL: return "null pointer argument";
+    case BSA_ERR_SHAPE: return "inconsistent sizes";
+    case BSA_ERR_LAYOUT_VALUE: return "layout value not 0 or 1";
+    case BSA_ERR_DTYPE: return "unsupported element type";
+    case BSA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case BSA_ERR_UNSUPPORTED: return "unsupported block/head-dim/order/scale";
+    case BSA_ERR_CUDA: return "CUDA call failed";
+    case BSA_ERR_DEVICE_TIMEOUT: return "bounded wait timed out on the device";
+    case BSA_ERR_STATE: return "LUT not uploaded to the current device";
+    case BSA_ERR_ALLOC: return "allocation failed";
+    default: return "unknown status";
+  }
+}
+
+const char* bsa_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// bsa_internal.h -- types shared by the host library and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+// The look-up table behind the opaque bsa_lut handle of bsa.h.
+struct bsa_lut {
+  int H = 0, nb = 0, batch = 0, order = 0;
+  int nnz_total = 0, n_items = 0;
+  std::vector<int32_t> row_ptr;  // [H*nb + 1]
+  std::vector<int32_t> col_idx;  // [nnz_total]
+  std::vector<int32_t> items;    // [n_items][4] = {b, h, i, nnz}
+  // device copies (valid after bsa_lut_upload)
+  int device = -1;
+  int32_t* d_row_ptr = nullptr;
+  int32_t* d_col_idx = nullptr;
+  int32_t* d_items = nullptr;
+  int32_t* d_status = nullptr;
+  uint64_t wait_limit_ns = 10000000000ull;
+};
+
+namespace bsa {
+
+// Kernel arguments besides the three tensor maps.
+struct FwdParams {
+  const int4* items;        // work list {b, h, i, nnz}
+  const int32_t* row_ptr;   // CSR row starts over rows h*nb + i
+  const int32_t* col_idx;   // active column blocks, ascending per row
+  void* out;                // bf16 [B,H,L,d]
+  float* lse;               // fp32 [B,H,L]
+  int32_t* status;          // device status word (0 = fine)
+  int n_items;
+  int H, L, nb;
+  float scale_log2;         // scale * log2(e)
+  int causal_diag;
+  unsigned long long wait_limit_ns;
+};
+
+// Wait-site ids recorded in the status word's low bits.
+enum WaitSite : int {
+  kSiteProdQEmpty = 1,
+  kSiteProdKEmpty = 2,
+  kSiteProdVEmpty = 3,
+  kSiteMmaQFull = 4,
+  kSiteMmaSEmpty = 5,
+  kSiteMmaKFull = 6,
+  kSiteMmaPFull = 7,
+  kSiteMmaVFull = 8,
+  kSiteSoftSFull = 9,
+  kSiteSoftOFull = 10,
+  kSiteSelftest = 15,
+};
+
+// One launcher per supported (block, head_dim) pair; each lives in its own
+// translation unit so the variants compile in parallel.
+cudaError_t launch_fwd_b128_d128(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                                 const CUtensorMap& v, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_b128_d64(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                                const CUtensorMap& v, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_b64_d128(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                                const CUtensorMap& v, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_b64_d64(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, int grid, cudaStream_t stream);
+
+// One-CTA kernel whose only wait never completes; it must give up after limit_ns.
+cudaError_t launch_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace bsa

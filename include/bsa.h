@@ -1,0 +1,175 @@
+/*
+ * bsa.h -- C ABI of libbsa: layout-driven block-sparse multi-head attention forward
+ * on GB300 (sm_103a).
+ *
+ * The operation.  A per-head int32 block layout [H x nb x nb] (nb = L / block) marks
+ * which block x block tiles of the attention matrix are computed: 1 = compute,
+ * 0 = skip (layout of the "Implementation:Deepspeedai DeepSpeed Sparse Attention
+ * Utils" page, "I/O Contract").  For batch b, head h and query row r the output is
+ * masked softmax attention over exactly the active keys
+ *
+ *     A(r)   = { c : layout[h][r/block][c/block] == 1,
+ *                    and not (causal_diag && r/block == c/block && c > r) }
+ *     s_c    = scale * <q[b,h,r,:], k[b,h,c,:]>
+ *     lse[r] = ln sum_{c in A(r)} exp(s_c)                (-inf when A(r) is empty)
+ *     O[r,:] = sum_{c in A(r)} exp(s_c - lse[r]) v[b,h,c,:]  (0 when A(r) is empty)
+ *
+ * i.e. dense attention (page "Block Sparse Attention Techniques", section 1,
+ * "Scaled Dot-Product Attention") under the elementwise mask that the block layout
+ * expands to (page "Block-Sparse Attention", section "Block Structure"; the masked
+ * scores are -inf as in the Longformer case-study equation of "Block Sparse
+ * Attention Techniques", section 2).  The online-softmax evaluation and the all-zero
+ * output of an empty row follow the sparse_attn kernel of the DeepSeek-V4.1
+ * "Sparse attention / Weighted row sum" page.
+ *
+ * Conventions shared by every call:
+ *   - Return value: BSA_OK (0) or a negative bsa_status.  No call aborts, throws or
+ *     prints.  Arguments are validated before any device work is queued.
+ *   - Tensors are dense, row-major, C-contiguous; "[B,H,L,d]" means element
+ *     (b,h,l,x) sits at ((b*H + h)*L + l)*d + x.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Device pointers must belong to the device that is current when the call is
+ *     made, the same device the LUT was uploaded to.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsa_status {
+  BSA_OK = 0,
+  BSA_ERR_NULL = -1,           /* a required pointer is NULL                           */
+  BSA_ERR_SHAPE = -2,          /* sizes inconsistent (L != nb*block, H/B vs the LUT...) */
+  BSA_ERR_LAYOUT_VALUE = -3,   /* a layout entry is neither 0 nor 1                    */
+  BSA_ERR_DTYPE = -4,          /* reserved for bindings that see element types          */
+  BSA_ERR_ALIGN = -5,          /* a tensor pointer is not 16-byte aligned              */
+  BSA_ERR_UNSUPPORTED = -6,    /* (block, d) pair or order flag not supported          */
+  BSA_ERR_CUDA = -7,           /* a CUDA runtime/driver call failed                    */
+  BSA_ERR_DEVICE_TIMEOUT = -8, /* a bounded wait inside the kernel ran out             */
+  BSA_ERR_STATE = -9,          /* the LUT has not been uploaded to a device            */
+  BSA_ERR_ALLOC = -10          /* host or device allocation failed                     */
+} bsa_status;
+
+/* Work-list orders accepted by bsa_build_lut. */
+enum {
+  BSA_ORDER_GLOBAL = 0,  /* items sorted by (-nnz, b, h, i): longest rows first           */
+  BSA_ORDER_GROUPED = 1  /* items sorted by (b, h, -nnz, i): one (b,h) at a time, K/V
+                            tiles stay hot in L2                                          */
+};
+
+/* Opaque look-up table: host CSR + work list, plus device copies after upload.
+ * Owned by the library; released by bsa_lut_free. */
+typedef struct bsa_lut bsa_lut;
+
+/*
+ * bsa_build_lut -- turn a block layout into a CSR of active column blocks and a
+ * load-balanced work list (host only; needs no GPU).
+ *
+ * CSR storage of the non-zero blocks follows "Block Sparse Attention Techniques",
+ * section 3.2, "Implementation with Sparse Matrix Formats".
+ *
+ *   layout  host, int32 [H, nb, nb], values 0/1, row-major; read only, not retained.
+ *   H, nb   heads and blocks per side (both >= 1; H*nb*nb < 2^31).
+ *   batch   batch size B the work list is built for (>= 1).
+ *   order   BSA_ORDER_GLOBAL or BSA_ORDER_GROUPED.
+ *   out     receives the new LUT (set to NULL on error).
+ *
+ * Contents (see bsa_lut_export): row_ptr int32[H*nb + 1] over rows r = h*nb + i,
+ * col_idx int32[nnz] with the active j of each row ascending, and items
+ * int32[B*H*nb][4] = {b, h, i, nnz of row (h,i)}, every (b,h,i) present once
+ * (zero-count items included), sorted stably by the order's key.
+ * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_LAYOUT_VALUE, BSA_ERR_UNSUPPORTED
+ * (bad order), BSA_ERR_ALLOC.
+ */
+int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bsa_lut** out);
+
+/*
+ * bsa_lut_info -- sizes of a LUT.  Any output pointer may be NULL.
+ * nnz_total = sum of the layout = length of col_idx; n_items = batch*H*nb.
+ */
+int bsa_lut_info(const bsa_lut* lut, int* H, int* nb, int* batch, int* nnz_total, int* n_items);
+
+/*
+ * bsa_lut_export -- copy the host CSR and work list into caller buffers of
+ * H*nb+1, nnz_total and 4*n_items int32 (any may be NULL to skip it).
+ */
+int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32_t* items);
+
+/*
+ * bsa_lut_upload -- allocate device copies of row_ptr, col_idx and the work list
+ * (plus a device status word) on the current device and copy them there on
+ * `stream`, then synchronize `stream`.  Call once before the first bsa_forward;
+ * calling again re-uploads to the now-current device.  Errors: BSA_ERR_NULL,
+ * BSA_ERR_ALLOC, BSA_ERR_CUDA.
+ */
+int bsa_lut_upload(bsa_lut* lut, void* stream);
+
+/* bsa_lut_free -- release host and device memory of a LUT (NULL is a no-op).  The
+ * caller makes sure no forward that uses it is still running. */
+void bsa_lut_free(bsa_lut* lut);
+
+/*
+ * bsa_forward -- O and lse of block-sparse attention (the operation above).
+ *
+ *   q, k, v  device, bf16 [B,H,L,d], 16-byte aligned, read only.
+ *   lut      uploaded LUT built for this (H, nb = L/block, batch = B).
+ *   out      device, bf16 [B,H,L,d], 16-byte aligned; every element written.
+ *   lse      device, fp32 [B,H,L], 16-byte aligned; natural-log log-sum-exp of the
+ *            scaled scores, -inf on rows without an active key.
+ *   scale    multiplies q.k before the softmax (any finite value, 0 included).
+ *   block    64 or 128; d (head dim) 64 or 128.  L must equal nb * block.
+ *   causal_diag  nonzero: inside diagonal blocks (row block == column block) key
+ *            c > query r is masked; other active blocks are not masked.
+ *   stream   cudaStream_t (void*) the kernel is queued on.
+ *
+ * Asynchronous: returns after queuing one kernel launch; allocates nothing and
+ * does not synchronize.  One forward per LUT may run at a time (the device status
+ * word is per LUT).  Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_ALIGN,
+ * BSA_ERR_UNSUPPORTED, BSA_ERR_STATE, BSA_ERR_CUDA (launch failure).
+ */
+int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
+                float* lse, int B, int H, int L, int d, float scale, int block, int causal_diag,
+                void* stream);
+
+/*
+ * bsa_device_status -- synchronize `stream`, read and clear the LUT's device status
+ * word.  Returns BSA_OK, or BSA_ERR_DEVICE_TIMEOUT if a bounded wait inside a
+ * kernel gave up since the last check (the kernel then skipped the remaining work
+ * and its outputs are undefined), or BSA_ERR_CUDA.  `detail` (may be NULL)
+ * receives the raw status word: wait-site id in the low 16 bits.
+ */
+int bsa_device_status(const bsa_lut* lut, void* stream, int32_t* detail);
+
+/*
+ * bsa_set_wait_limit -- per-wait time limit, in nanoseconds, that kernels queued
+ * after this call use for every barrier wait (default 1e10 = 10 s; 0 restores the
+ * default).  A wait that runs out records BSA_ERR_DEVICE_TIMEOUT in the status word
+ * and the kernel returns instead of hanging.
+ */
+int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns);
+
+/*
+ * bsa_wait_selftest -- launch a one-CTA kernel that waits on a shared-memory
+ * barrier nothing ever signals, bounded by `limit_ns`, and report what the
+ * kernel recorded: BSA_ERR_DEVICE_TIMEOUT when the bounded wait fired as
+ * designed (the expected result), BSA_OK if it did not.  Synchronizes `stream`.
+ * This exercises the timeout path of every wait in the forward kernel without a
+ * fault or a hang.
+ */
+int bsa_wait_selftest(uint64_t limit_ns, void* stream);
+
+/* bsa_status_string -- static English text for a status code. */
+const char* bsa_status_string(int status);
+
+/* bsa_version -- library version string ("major.minor.patch"). */
+const char* bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

@@ -1,0 +1,129 @@
+"""C-ABI library on the CPU: exported symbols, bit-exact LUT / work list against the
+oracle, and argument validation (no device work: every checked call fails before it
+would touch a GPU)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import block_sparse_head_gb300 as bsa
+from block_sparse_head_gb300 import binding
+from block_sparse_head_gb300 import workloads as wls
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "bsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bsa.library_path()):
+        from block_sparse_head_gb300 import build as b
+
+        b.build()
+    return bsa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.EXPORTED)
+    assert lib.bsa_version().decode().count(".") == 2
+
+
+def test_status_strings(lib):
+    for code in range(0, -11, -1):
+        s = lib.bsa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.bsa_status_string(-99).decode() == "unknown status"
+
+
+def _compare(layout, batch, order):
+    lut = bsa.build_lut(layout, batch, order, upload=False)
+    rp, ci, it = lut.export()
+    orp, oci, oit = oracle.oracle_lut(np.asarray(layout), batch, order)
+    assert np.array_equal(rp, orp)
+    assert np.array_equal(ci, oci)
+    assert np.array_equal(it, oit)
+    assert lut.nnz_total == oci.size and lut.n_items == oit.shape[0]
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("order", ["global", "grouped"])
+def test_lut_bit_exact_workloads(lib, index, order):
+    wl = wls.WORKLOADS[index]
+    _compare(wls.layout_for(wl).numpy(), wl.B, order)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_lut_bit_exact_random(lib, seed):
+    rng = np.random.default_rng(seed)
+    H, nb, B = int(rng.integers(1, 5)), int(rng.integers(1, 20)), int(rng.integers(1, 4))
+    lay = wls.random_layout(H, nb, float(rng.uniform(0.0, 1.0)), seed,
+                            empty_rows=int(rng.integers(0, nb + 1))).numpy()
+    for order in ("global", "grouped"):
+        _compare(lay, B, order)
+
+
+def test_lut_degenerate(lib):
+    for lay in (np.zeros((2, 3, 3), np.int32), np.ones((1, 1, 1), np.int32),
+                np.ones((3, 5, 5), np.int32), np.eye(7, dtype=np.int32)[None]):
+        for order in ("global", "grouped"):
+            _compare(lay, 2, order)
+
+
+def _build_status(lib, lay, H, nb, batch, order=0):
+    h = ctypes.c_void_p()
+    arr = None if lay is None else np.ascontiguousarray(lay, dtype=np.int32)
+    st = lib.bsa_build_lut(None if arr is None else arr.ctypes.data, H, nb, batch, order,
+                           ctypes.byref(h))
+    if h.value:
+        lib.bsa_lut_free(h)
+    return st, h.value
+
+
+def test_build_lut_errors(lib):
+    ones = np.ones((1, 2, 2), np.int32)
+    assert _build_status(lib, None, 1, 2, 1) == (-1, None)
+    assert _build_status(lib, ones, 0, 2, 1)[0] == -2
+    assert _build_status(lib, ones, 1, 0, 1)[0] == -2
+    assert _build_status(lib, ones, 1, 2, 0)[0] == -2
+    assert _build_status(lib, ones, 1, 2, 1, order=7)[0] == -6
+    bad = ones.copy()
+    bad[0, 1, 0] = 2
+    assert _build_status(lib, bad, 1, 2, 1)[0] == -3
+    bad[0, 1, 0] = -1
+    assert _build_status(lib, bad, 1, 2, 1)[0] == -3
+    assert lib.bsa_build_lut(ones.ctypes.data, 1, 2, 1, 0, None) == -1
+    with pytest.raises(binding.BsaError):
+        bsa.build_lut(bad, 1, upload=False)
+
+
+def test_forward_validation_before_device_work(lib):
+    """Every rejected call returns before touching a device; pointers here are fake."""
+    lut = bsa.build_lut(np.ones((2, 4, 4), np.int32), 1, upload=False)
+    A = 1 << 20  # fake, 16-byte aligned, never dereferenced
+    f = lambda **kw: lib.bsa_forward(  # noqa: E731
+        kw.get("q", A), kw.get("k", A), kw.get("v", A), kw.get("lut", lut.handle),
+        kw.get("out", A), kw.get("lse", A), kw.get("B", 1), kw.get("H", 2), kw.get("L", 256),
+        kw.get("d", 64), ctypes.c_float(kw.get("scale", 0.125)), kw.get("block", 64),
+        kw.get("causal", 0), None)
+    assert f(q=None) == -1 and f(lut=None) == -1 and f(lse=None) == -1
+    assert f(block=32) == -6 and f(d=96) == -6 and f(scale=float("nan")) == -6
+    assert f(B=2) == -2 and f(H=3) == -2 and f(L=512) == -2
+    assert f(block=128, L=256) == -2  # nb = 4 blocks of 128 != 256
+    assert f(q=A + 8) == -5 and f(out=A + 2) == -5 and f(lse=A + 4) == -5
+    assert f() == -9  # valid arguments, but the LUT was never uploaded
+    assert lib.bsa_device_status(lut.handle, None, None) == -9
+    assert lib.bsa_set_wait_limit(None, 5) == -1
+    assert lib.bsa_lut_info(None, None, None, None, None, None) == -1
