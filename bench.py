@@ -1,0 +1,407 @@
+"""Benchmark of the block-sparse attention forward (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl reference]
+
+A step is one ``bsa_forward`` over one batch of the workload (one kernel launch).
+The default workload is 5 (B=1, H=32, L=65536, block 128, d 128, Sparse-Transformer
+layout, causal diagonal): the largest of the five and one of the three the 55%-of-peak
+target names.  ``value`` is active-block TFLOPS (4 * block^2 * d per active block per
+batch entry) over the whole job, timed with CUDA events on the launching stream.
+Under torchrun every rank runs its own replica of the workload (weak scaling) and the
+slowest rank's time counts.
+
+``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the same
+workload (query blocks taken in work-list order), on this host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn fwd active-block TFLOPS and % of GB300 bf16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["bsa_fwd_kernel.cuh", "bsa_ptx.cuh", "bsa_host.cpp", "bsa_internal.h"]
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_head_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"bsa_fwd_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_per_launch_bytes\s*=\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_sources_sha256\s*=\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != kernel_sources_sha():
+        return None
+    return float(m_t.group(1))
+
+
+# ----------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def _oracle_sample_worker(index: int, budget_s: float, steps: int, warmup: int,
+                          per_step_items: int) -> dict:
+    """Runs in a fresh interpreter: times the oracle on query blocks of the workload."""
+    import numpy as np
+
+    import oracle
+    from block_sparse_head_gb300 import workloads as wls
+
+    wl = wls.WORKLOADS[index]
+    lay = wls.layout_for(wl).numpy()
+    row_ptr, col_idx, items = oracle.oracle_lut(lay, wl.B)
+    # bf16 -> fp32 is exact; the oracle gathers each item's rows and computes in fp64.
+    q, k, v = (t.float().numpy() for t in wls.qkv(wl))
+    t_load = time.time()
+    step_times, step_flops = [], []
+    pos = 0
+    total_steps = warmup + steps
+    t_begin = time.time()
+    for s in range(total_steps):
+        t0 = time.perf_counter()
+        flops = 0
+        for _ in range(per_step_items):
+            b, h, i, nnz = (int(x) for x in items[pos % len(items)])
+            pos += 1
+            oracle.query_block(q[b, h], k[b, h], v[b, h], lay[h], wl.scale, wl.block,
+                               wl.causal_diag, i)
+            flops += 4 * wl.block * wl.block * wl.d * nnz
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            step_times.append(dt)
+            step_flops.append(flops)
+        if budget_s and time.time() - t_begin > budget_s and s >= warmup:
+            break
+    tot_t = sum(step_times)
+    return {"tflops": sum(step_flops) / tot_t / 1e12 if tot_t > 0 else 0.0,
+            "steps_timed": len(step_times), "items_per_step": per_step_items,
+            "seconds": tot_t, "ms_per_step": 1e3 * tot_t / max(1, len(step_times)),
+            "setup_s": t_load - t_begin}
+
+
+def run_oracle_subprocess(index: int, budget_s: float, steps: int, warmup: int,
+                          per_step_items: int) -> dict:
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = (f"import json,sys; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench._oracle_sample_worker({index}, {budget_s}, {steps}, "
+            f"{warmup}, {per_step_items})))")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed:\n{r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["cores"] = cores
+    return res
+
+
+# ------------------------------------------------------------------- GPU arm
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(wl, l2_note: str, world: int) -> dict:
+    return {"workload": f"{wl.name} (workload {wl.index})", "batch": wl.B, "heads": wl.H,
+            "seq_len": wl.L, "block": wl.block, "head_dim": wl.d,
+            "causal_diag": bool(wl.causal_diag), "layout": wl.name, "l2": l2_note,
+            "parallelism": "replicas" if world > 1 else "single-gpu"}
+
+
+def gpu_arm(args) -> None:
+    import numpy as np  # noqa: F401
+    import torch
+
+    import block_sparse_head_gb300 as bsa
+    from block_sparse_head_gb300 import binding
+    from block_sparse_head_gb300 import workloads as wls
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    wl = wls.WORKLOADS[args.workload]
+    lay = wls.layout_for(wl)
+    flops_step = 4 * wl.block * wl.block * wl.d * int(lay.sum()) * wl.B
+    q, k, v = wls.qkv(wl)
+    in_bytes = 3 * q.numel() * 2
+    lut = bsa.build_lut(lay, wl.B, args.order)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    out = torch.empty_like(qd)
+    lse = torch.empty(wl.B, wl.H, wl.L, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    flush = None
+    l2_note = "inputs larger than L2"
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+        l2_note = "L2 flushed between steps (256 MiB write, outside the events)"
+
+    def step():
+        bsa.forward(qd, kd, vd, lut, wl.scale, wl.block, wl.causal_diag, out=out, lse=lse,
+                    stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    st, word = lut.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({word:#x}) during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)  # let the sampler start
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        if flush is not None:
+            flush.fill_(s)
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if pg:
+        pg.barrier()
+    clk = clocks.stop() if clocks else None
+    per_step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    local_ms = sum(per_step_ms)
+    st, word = lut.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({word:#x}) in the timed region")
+
+    # e2e: host (pinned) buffers through the same C-ABI call, copies inside the region.
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    lh = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
+    bufs = (qd, kd, vd, out, lse)
+    for _ in range(2):
+        binding.forward_host(qh, kh, vh, lut, wl.scale, wl.block, wl.causal_diag, out=oh, lse=lh,
+                             dev_bufs=bufs, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        binding.forward_host(qh, kh, vh, lut, wl.scale, wl.block, wl.causal_diag, out=oh, lse=lh,
+                             dev_bufs=bufs, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms_local = e0.elapsed_time(e1)
+
+    if pg:
+        t = torch.tensor([local_ms, e2e_ms_local], device="cuda", dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        local_ms, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = e2e_ms_local
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    ms_per_step = local_ms / args.steps
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    peaks = measured_peaks()
+    peak_kind = "bf16_burst" if local_ms < 3000 else "bf16_sustained"
+    peak = peaks[peak_kind]
+    achieved = flops_step / (statistics.mean(per_step_ms) * 1e-3) / 1e12
+    traffic = recorded_traffic(wl.name)
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16; layouts generated from seeds)",
+        "config": workload_config(wl, l2_note, world),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peaks['source']} {peak_kind} (MEASURED_PEAKS.json)",
+                     "traffic": traffic, "flops_per_launch": flops_step},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
+                "steps": e2e_steps, "ms_per_step": round(e2e_ms / e2e_steps, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+        "order": args.order,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        cb = run_oracle_subprocess(wl.index, args.cpu_budget, 10 ** 6, 1, args.cpu_items)
+        line["cpu_baseline"] = {
+            "value": round(cb["tflops"], 6), "unit": "TFLOPS", "cores": cb["cores"],
+            "kind": "oracle",
+            "sample": (f"{cb['steps_timed'] * cb['items_per_step']} query blocks of the workload "
+                       f"in work-list order (longest rows first), {cb['seconds']:.1f} s of fp64 "
+                       "numpy oracle on the host cores")}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def reference_arm(args) -> None:
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from block_sparse_head_gb300 import workloads as wls
+
+    wl = wls.WORKLOADS[args.workload]
+    res = run_oracle_subprocess(wl.index, 0.0, args.steps, args.warmup, args.ref_items)
+    line = {
+        "metric": METRIC,
+        "value": round(res["tflops"], 6),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["ms_per_step"], 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16; layouts generated from seeds)",
+        "config": workload_config(wl, "host CPU (no GPU)", 1),
+        "impl": "reference",
+        "cpu_baseline": {"value": round(res["tflops"], 6), "unit": "TFLOPS", "cores": res["cores"],
+                         "kind": "oracle",
+                         "sample": (f"each step = {res['items_per_step']} query blocks of the "
+                                    "workload in work-list order, fp64 numpy oracle")},
+        "e2e": {"value": round(res["tflops"], 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--order", default="global", choices=["global", "grouped"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    ap.add_argument("--cpu-items", type=int, default=8, help="query blocks per oracle step")
+    ap.add_argument("--ref-items", type=int, default=4, help="query blocks per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -209,9 +209,9 @@ def query_block(q_bh, k_bh, v_bh, layout_h, scale: float, block: int,
     mask = np.ones((block, cols.size), dtype=bool)
     if causal_diag:
         mask &= ~((cols[None, :] // block == i) & (cols[None, :] > rows[:, None]))
-    qb = np.asarray(q_bh, dtype=np.float64)[rows]
-    kb = np.asarray(k_bh, dtype=np.float64)[cols]
-    vb = np.asarray(v_bh, dtype=np.float64)[cols]
+    qb = np.asarray(q_bh)[rows].astype(np.float64)
+    kb = np.asarray(k_bh)[cols].astype(np.float64)
+    vb = np.asarray(v_bh)[cols].astype(np.float64)
     return masked_attention(qb, kb, vb, mask, scale)
 
 
