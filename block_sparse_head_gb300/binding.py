@@ -27,7 +27,7 @@ BSA_ERR_DEVICE_TIMEOUT = -8
 EXPORTED = (
     "bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_upload", "bsa_lut_free",
     "bsa_forward", "bsa_device_status", "bsa_set_wait_limit", "bsa_wait_selftest",
-    "bsa_status_string", "bsa_version",
+    "bsa_status_string", "bsa_version", "bsa_forward_noalloc",
 )
 
 _lib = None
@@ -70,6 +70,10 @@ def load_library():
         lib.bsa_forward.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                     ctypes.c_int, vp]
+        lib.bsa_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                            ctypes.c_int, ctypes.c_int, vp, ctypes.c_int]
+        lib.bsa_forward_noalloc.restype = ctypes.c_int
         lib.bsa_device_status.argtypes = [vp, vp, i32p]
         lib.bsa_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
         lib.bsa_wait_selftest.argtypes = [ctypes.c_uint64, vp]

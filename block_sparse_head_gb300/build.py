@@ -26,6 +26,7 @@ SOURCES = [
     "bsa_fwd_b128_d64.cu",
     "bsa_fwd_b64_d128.cu",
     "bsa_fwd_b64_d64.cu",
+    "bsa_noalloc.cu",
 ]
 HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_fwd_kernel.cuh"]
 

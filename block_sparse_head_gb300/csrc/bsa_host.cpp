@@ -304,6 +304,7 @@ const char* bsa_status_string(int status) {
     case BSA_ERR_DEVICE_TIMEOUT: return "bounded wait timed out on the device";
     case BSA_ERR_STATE: return "LUT not uploaded to the current device";
     case BSA_ERR_ALLOC: return "allocation failed";
+    case BSA_ERR_TOO_LARGE: return "LUT too large for the fixed 4 MiB no-allocation scratch";
     default: return "unknown status";
   }
 }

@@ -51,7 +51,9 @@ typedef enum bsa_status {
   BSA_ERR_CUDA = -7,           /* a CUDA runtime/driver call failed                    */
   BSA_ERR_DEVICE_TIMEOUT = -8, /* a bounded wait inside the kernel ran out             */
   BSA_ERR_STATE = -9,          /* the LUT has not been uploaded to a device            */
-  BSA_ERR_ALLOC = -10          /* host or device allocation failed                     */
+  BSA_ERR_ALLOC = -10,         /* host or device allocation failed                     */
+  BSA_ERR_TOO_LARGE = -11      /* LUT does not fit the fixed scratch of
+                                  bsa_forward_noalloc                                   */
 } bsa_status;
 
 /* Work-list orders accepted by bsa_build_lut. */
@@ -134,6 +136,37 @@ void bsa_lut_free(bsa_lut* lut);
 int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
                 float* lse, int B, int H, int L, int d, float scale, int block, int causal_diag,
                 void* stream);
+
+/*
+ * bsa_forward_noalloc -- the same forward as bsa_forward for callers that cannot
+ * allocate device memory.  The pages have no counterpart of this call.
+ *
+ * Some callers may not call cudaMalloc at all: code running inside a host callback
+ * or a plugin hook where allocating could deadlock or is forbidden, code under a
+ * memory manager that owns the whole device heap, or a process that must not grow
+ * its device footprint after start-up.  They build the LUT on the host with
+ * bsa_build_lut (host memory only; no bsa_lut_upload needed) and pass their own q,
+ * k, v, out and lse buffers, exactly as for bsa_forward.  The LUT's device copy and
+ * the device status word go into one fixed 4 MiB array that is part of the library
+ * image (every GPU that loads the library holds it until the process exits); this
+ * call calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments q ... stream: as bsa_forward (`lut` need not be uploaded).
+ *   sync_status  0: asynchronous, device timeouts are not reported.  Nonzero: the
+ *                call synchronizes `stream` after the kernel and returns
+ *                BSA_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel gave up.
+ *
+ * Limit: 4 + 4*n_items + (H*nb + 1) + nnz int32 words (each part rounded up to 4
+ * words) must fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before any
+ * device work.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture.  All calls share the array and each call overwrites it: calls
+ * whose kernels overlap on the GPU (other streams, other host threads) race, so
+ * serialize them on one stream.  Other errors: as bsa_forward.
+ */
+int bsa_forward_noalloc(const void* q, const void* k, const void* v, const bsa_lut* lut,
+                        void* out, float* lse, int B, int H, int L, int d, float scale, int block,
+                        int causal_diag, void* stream, int sync_status);
 
 /*
  * bsa_device_status -- synchronize `stream`, read and clear the LUT's device status
