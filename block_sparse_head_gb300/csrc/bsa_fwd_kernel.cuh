@@ -8,24 +8,32 @@
 // Techniques" (sections 3.2 and 4) and the DeepSpeed sparse-attention utils page.
 // Scores outside the active blocks are never formed: their exp() would be 0.
 //
-// GB300 mapping (one CTA per SM, 256 threads, warp-specialised):
-//   warp 0       TMA producer: Q tile once per item, K and V tiles of each active
-//                block into two rings of kStages slots (128-byte swizzled boxes).
-//   warp 1       tcgen05 issuer (one thread) and TMEM owner:
-//                  S = Q K^T   (M = block, N = block, K = d) into one of two TMEM
-//                              S buffers, so S(j+1) runs while softmax works on S(j);
-//                  O += P V    (M = block, N = d, K = block) into the TMEM O tile,
-//                              P from shared memory, V as an MN-major operand.
-//   warps 4..7   softmax warpgroup: TMEM -> registers, causal mask on the diagonal
-//                block, base-2 online softmax with a lazy rescale (the running max is
-//                only moved when it grows by more than 2^8), P -> shared memory as
-//                bf16, O rescale in TMEM when needed, and the epilogue (O / l -> bf16,
-//                lse = ln 2 * (m + log2 l)).  An item with no active block writes
-//                O = 0 and lse = -inf.
-//   warps 2..3   idle.
-// Block 128 uses M = 128 MMAs (row r of S/O in TMEM lane r, one thread per row);
-// block 64 uses M = 64 MMAs, whose rows sit in lanes 0-15 of each 32-lane quadrant,
-// and each row is split between lanes t and t+16 of a warp (16x32bx2 TMEM loads).
+// Keys are consumed in steps of 128 rows: one block when b = 128, the next two active
+// blocks of the row when b = 64 (the last step of a row with an odd count holds one).
+//
+// GB300 mapping.  One CTA per SM, 384 threads, two work items in flight per CTA
+// ("slots" 0 and 1, each with its own Q tile, TMEM S/P and O, and softmax warpgroup),
+// so the tensor core runs one slot's MMAs while the other slot's softmax runs:
+//   warp 0        TMA producer: Q tile of each item into its slot's Q buffer (and an
+//                 L2 prefetch of the slot's next Q), K and V step tiles into one ring
+//                 of kRing slots, in exactly the order the MMA warp consumes them.
+//   warp 1        tcgen05 issuer (one thread) and TMEM owner.  Per slot, alternating:
+//                   O += P V   (M = b, N = d, K = keys; A = P read from TMEM)
+//                   S = Q K^T  (M = b, N = keys, K = d; into the slot's TMEM S, which
+//                              P overwrites in place once the softmax has read S)
+//   warps 4..7    softmax warpgroup of slot 0; warps 8..11 that of slot 1: TMEM ->
+//                 registers, causal mask on diagonal blocks, base-2 online softmax
+//                 (exp2(s*c - m) with c = scale*log2(e) in one FFMA, tree reductions),
+//                 lazy rescale (the running max moves only when it grows by more than
+//                 2^8; O is rescaled in TMEM, which is safe because S(j) completing
+//                 implies PV(j-1) completed), P -> TMEM as bf16, and the epilogue
+//                 (O / l -> bf16, lse = ln 2 * (m + log2 l)); an item with no active
+//                 block writes O = 0 and lse = -inf.
+//   warps 2..3    idle.
+// b = 128 uses M = 128 MMAs (row r of S/P/O in TMEM lane r, one thread per row);
+// b = 64 uses M = 64 MMAs, whose rows sit in lanes 0-15 of each 32-lane quadrant:
+// lanes t and t+16 of a warp share a row, each holding one of the step's two key
+// blocks (16x32bx2 TMEM loads and stores).
 //
 // Every barrier wait is bounded (WaitCtl): a wait that runs out records a timeout in
 // the status word, and all roles leave their loops, drain in-flight copies and MMAs,
@@ -43,35 +51,39 @@ template <int BLK, int D>
 struct FwdCfg {
   static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-  static constexpr int kThreads = 256;
-  static constexpr int kTile = BLK * D * 2;  // bytes of one Q, K or V tile
-  static constexpr int kStages = kTile >= 32768 ? 2 : (kTile >= 16384 ? 3 : 4);
-  static constexpr int kPBytes = BLK * BLK * 2;
-  static constexpr int kRegion = BLK * 128;  // one 64-column swizzled box of BLK rows
-  static constexpr int kSCols = BLK;         // TMEM columns of one S buffer
-  static constexpr int kOCol = 2 * kSCols;   // TMEM column of the O tile
-  static constexpr int kTmemCols = (2 * kSCols + D) <= 256 ? 256 : 512;
+  static constexpr int kThreads = 384;
+  static constexpr int kKR = 128;                 // key rows per step
+  static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
+  static constexpr int kQTile = BLK * D * 2;      // bytes of one Q tile
+  static constexpr int kKVTile = kKR * D * 2;     // bytes of one K or V step tile
+  static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
+  static constexpr int kKVRegion = kKR * 128;     // one 64-column box of a step tile
+  static constexpr int kSlotCols = 256;           // TMEM columns per slot: S/P then O
+  static constexpr int kOCol = 128;               // O offset inside a slot
+  static constexpr int kTmemCols = 512;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTile;
-  static constexpr int kOffV = kOffK + kStages * kTile;
-  static constexpr int kOffP = kOffV + kStages * kTile;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffRing = kOffQ + 2 * kQTile;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kRingFit = (232448 - 1024 - kBarBytes - kOffRing) / kKVTile;
+  static constexpr int kRing = kRingFit < 8 ? kRingFit : 8;
+  static constexpr int kOffBar = kOffRing + kRing * kKVTile;
   // barrier indices
-  static constexpr int kBarQF = 0, kBarQE = 1;
-  static constexpr int kBarKF = 2;
-  static constexpr int kBarKE = kBarKF + kStages;
-  static constexpr int kBarVF = kBarKE + kStages;
-  static constexpr int kBarVE = kBarVF + kStages;
-  static constexpr int kBarSF = kBarVE + kStages;
-  static constexpr int kBarSE = kBarSF + 2;
-  static constexpr int kBarPF = kBarSE + 2;
-  static constexpr int kBarOF = kBarPF + 1;
-  static constexpr int kBarDrain = kBarOF + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + align slack
+  static constexpr int kBarQF = 0;                // [2] per slot
+  static constexpr int kBarQE = 2;                // [2]
+  static constexpr int kBarSF = 4;                // [2]
+  static constexpr int kBarPF = 6;                // [2]
+  static constexpr int kBarOF = 8;                // [2]
+  static constexpr int kBarDrain = 10;
+  static constexpr int kBarRF = 11;               // [kRing] ring full
+  static constexpr int kBarRE = kBarRF + kRing;   // [kRing] ring empty
+  static constexpr int kNumBars = kBarRE + kRing;
+  static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
+  static_assert(kRing >= 4, "ring too small");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // instruction descriptors
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(BLK, BLK, false, false);
+  // instruction descriptors: S over a full step (N = 128) or a single 64-key block
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(BLK, kKR, false, false);
+  static constexpr uint32_t kIdescS1 = idesc_bf16_f32(BLK, BLK, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BLK, D, false, true);
 };
 
@@ -88,11 +100,65 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
+// Blocks in step s of a row with nnz active blocks.
+template <int G>
+__device__ __forceinline__ int step_blocks(int nnz, int s) {
+  const int rem = nnz - s * G;
+  return rem < G ? rem : G;
+}
+
+// Slot X of a CTA owns positions k = X, X+2, X+4, ... of the CTA's round-robin share
+// of the work list (item blockIdx.x + k * gridDim.x).  Advances k to the next
+// non-empty item at or after k; false when the share is exhausted.
+__device__ __forceinline__ bool seek_item(const FwdParams& p, int& k, int4& item) {
+  for (;; k += 2) {
+    const int t = blockIdx.x + k * gridDim.x;
+    if (t >= p.n_items) return false;
+    item = p.items[t];
+    if (item.w > 0) return true;
+  }
+}
+
+// The consumption schedule shared by the producer and the MMA warp.  Slots take
+// turns; a turn of slot X is: PV of X's pending step (if any), then S of X's next
+// step (the next item's step 0 when the current item is exhausted).  Each action
+// uses one ring tile (V for PV, K for S), so both warps see the same ring order.
+// on_pv(X, item, step, nblk, last_step) / on_s(X, item, step, nblk, k) return false
+// to stop early.
+template <int G, class OnPV, class OnS>
+__device__ __forceinline__ void walk_schedule(const FwdParams& p, OnPV&& on_pv, OnS&& on_s) {
+  int k[2] = {0, 1};
+  int4 it[2];
+  int nsteps[2], s_next[2] = {0, 0}, pend[2] = {-1, -1};
+  bool done[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    done[x] = !seek_item(p, k[x], it[x]);
+    nsteps[x] = done[x] ? 0 : (it[x].w + G - 1) / G;
+  }
+  while (!(done[0] && done[1])) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (done[x]) continue;
+      if (pend[x] >= 0) {
+        if (!on_pv(x, it[x], pend[x], step_blocks<G>(it[x].w, pend[x]), pend[x] == nsteps[x] - 1))
+          return;
+        pend[x] = -1;
+      }
+      if (s_next[x] >= nsteps[x]) {
+        k[x] += 2;
+        if (!seek_item(p, k[x], it[x])) {
+          done[x] = true;
+          continue;
+        }
+        nsteps[x] = (it[x].w + G - 1) / G;
+        s_next[x] = 0;
+      }
+      const int s = s_next[x]++;
+      if (!on_s(x, it[x], s, step_blocks<G>(it[x].w, s), k[x])) return;
+      pend[x] = s;
+    }
+  }
 }
 
 // ----------------------------------------------------------------- producer
@@ -102,58 +168,63 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
-  constexpr int S = C::kStages;
+  constexpr int R = C::kRing;
+  constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  int qc = 0, kc = 0, vc = 0;
-  bool ok = true;
-  for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
-    const int4 it = p.items[t];
-    const int nnz = it.w;
-    if (nnz == 0) continue;
+  int qc[2] = {0, 0};
+  int rc = 0;
+
+  // Loads the K or V rows of one step into the next ring tile.
+  auto load_step = [&](const CUtensorMap* tm, const int4& it, int step, int nblk) -> bool {
+    const int r = rc % R;
+    if (!mbar_wait(bar(C::kBarRE + r), ((rc / R) & 1) ^ 1, ctl, kSiteProdRingEmpty)) return false;
     const int rowbase = (it.x * p.H + it.y) * p.L;
-    const int start = p.row_ptr[it.y * p.nb + it.z];
-    ok = mbar_wait(bar(C::kBarQE), (qc & 1) ^ 1, ctl, kSiteProdQEmpty);
-    if (!ok) break;
-    mbar_arrive_expect_tx(bar(C::kBarQF), C::kTile);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c)
-      tma_load_2d(sbase + C::kOffQ + c * C::kRegion, tm_q, bar(C::kBarQF), c * 64,
-                  rowbase + it.z * BLK);
-    ++qc;
-    for (int j = 0; j < nnz; ++j) {
-      const int krow = rowbase + p.col_idx[start + j] * BLK;
-      const int ks = kc % S;
-      ok = mbar_wait(bar(C::kBarKE + ks), ((kc / S) & 1) ^ 1, ctl, kSiteProdKEmpty);
-      if (!ok) break;
-      mbar_arrive_expect_tx(bar(C::kBarKF + ks), C::kTile);
+    const int* cols = p.col_idx + p.row_ptr[it.y * p.nb + it.z] + step * G;
+    mbar_arrive_expect_tx(bar(C::kBarRF + r), nblk * BLK * D * 2);
+    for (int g = 0; g < nblk; ++g) {
+      const int krow = rowbase + cols[g] * BLK;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sbase + C::kOffK + ks * C::kTile + c * C::kRegion, tm_k, bar(C::kBarKF + ks),
-                    c * 64, krow);
-      ++kc;
-      const int vs = vc % S;
-      ok = mbar_wait(bar(C::kBarVE + vs), ((vc / S) & 1) ^ 1, ctl, kSiteProdVEmpty);
-      if (!ok) break;
-      mbar_arrive_expect_tx(bar(C::kBarVF + vs), C::kTile);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sbase + C::kOffV + vs * C::kTile + c * C::kRegion, tm_v, bar(C::kBarVF + vs),
-                    c * 64, krow);
-      ++vc;
+        tma_load_2d(sbase + C::kOffRing + r * C::kKVTile + c * C::kKVRegion + g * BLK * 128, tm,
+                    bar(C::kBarRF + r), c * 64, krow);
     }
-  }
+    ++rc;
+    return true;
+  };
+
+  walk_schedule<G>(
+      p,
+      [&](int x, const int4& it, int step, int nblk, bool) { return load_step(tm_v, it, step, nblk); },
+      [&](int x, const int4& it, int step, int nblk, int k) {
+        if (step == 0) {
+          if (!mbar_wait(bar(C::kBarQE + x), (qc[x] & 1) ^ 1, ctl, kSiteProdQEmpty)) return false;
+          mbar_arrive_expect_tx(bar(C::kBarQF + x), C::kQTile);
+          const int qrow = (it.x * p.H + it.y) * p.L + it.z * BLK;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(sbase + C::kOffQ + x * C::kQTile + c * C::kQRegion, tm_q,
+                        bar(C::kBarQF + x), c * 64, qrow);
+          ++qc[x];
+          // Warm L2 with the slot's next Q tile.
+          int k2 = k + 2;
+          int4 nxt;
+          if (seek_item(p, k2, nxt)) {
+            const int nrow = (nxt.x * p.H + nxt.y) * p.L + nxt.z * BLK;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(tm_q, c * 64, nrow);
+          }
+        }
+        return load_step(tm_k, it, step, nblk);
+      });
+
   // Wait until every copy this thread issued has landed (immediate on the normal path).
-  if (qc > 0) mbar_drain_wait(bar(C::kBarQF), (qc - 1) & 1);
-  for (int s = 0; s < S; ++s) {
-    if (kc > s) {
-      const int f = s + S * ((kc - 1 - s) / S);
-      mbar_drain_wait(bar(C::kBarKF + s), (f / S) & 1);
+  for (int x = 0; x < 2; ++x)
+    if (qc[x] > 0) mbar_drain_wait(bar(C::kBarQF + x), (qc[x] - 1) & 1);
+  for (int r = 0; r < R; ++r)
+    if (rc > r) {
+      const int f = r + R * ((rc - 1 - r) / R);
+      mbar_drain_wait(bar(C::kBarRF + r), (f / R) & 1);
     }
-    if (vc > s) {
-      const int f = s + S * ((vc - 1 - s) / S);
-      mbar_drain_wait(bar(C::kBarVF + s), (f / S) & 1);
-    }
-  }
 }
 
 // --------------------------------------------------------------- MMA issuer
@@ -162,70 +233,59 @@ template <int BLK, int D>
 __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                         const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
-  constexpr int S = C::kStages;
+  constexpr int R = C::kRing;
+  constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  int qc = 0, kc = 0, vc = 0, sc = 0, pc = 0;
-  bool ok = true;
+  int qc[2] = {0, 0}, pc[2] = {0, 0};
+  int rc = 0;
 
-  // S(sc) = Q K(kc)^T into TMEM buffer sc & 1.
-  auto issue_s = [&]() -> bool {
-    const int sb = sc & 1;
-    if (!mbar_wait(bar(C::kBarSE + sb), ((sc >> 1) & 1) ^ 1, ctl, kSiteMmaSEmpty)) return false;
-    const int ks = kc % S;
-    if (!mbar_wait(bar(C::kBarKF + ks), (kc / S) & 1, ctl, kSiteMmaKFull)) return false;
-    tc_fence_after();
-    const uint32_t qa = sbase + C::kOffQ;
-    const uint32_t ka = sbase + C::kOffK + ks * C::kTile;
+  walk_schedule<G>(
+      p,
+      // O_x (+)= P_x V : P from the slot's TMEM S columns, V from the ring.
+      [&](int x, const int4&, int step, int nblk, bool last) -> bool {
+        if (!mbar_wait(bar(C::kBarPF + x), pc[x] & 1, ctl, kSiteMmaPFull)) return false;
+        ++pc[x];
+        const int r = rc % R;
+        if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
+        tc_fence_after();
+        const uint32_t ts = tmem + x * C::kSlotCols;
+        const uint32_t va = sbase + C::kOffRing + r * C::kKVTile;
+        const int ksteps = nblk * BLK / 16;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * C::kRegion + (kk & 3) * 32;
-      tc_mma_ss(tmem + sb * C::kSCols, sdesc_sw128(qa + off, 16, 1024),
-                sdesc_sw128(ka + off, 16, 1024), C::kIdescS, kk > 0);
-    }
-    tc_commit(bar(C::kBarKE + ks));
-    tc_commit(bar(C::kBarSF + sb));
-    ++kc;
-    ++sc;
-    return true;
-  };
+        for (int kk = 0; kk < C::kKR / 16; ++kk)
+          if (kk < ksteps)
+            tc_mma_ts(ts + C::kOCol, ts + kk * 8, sdesc_sw128(va + kk * 16 * 128, C::kKVRegion, 1024),
+                      C::kIdescPV, (step > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::kBarRE + r));
+        if (last) tc_commit(bar(C::kBarOF + x));
+        ++rc;
+        return true;
+      },
+      // S_x = Q_x K^T into the slot's TMEM S columns.
+      [&](int x, const int4& it, int step, int nblk, int) -> bool {
+        if (step == 0) {
+          if (!mbar_wait(bar(C::kBarQF + x), qc[x] & 1, ctl, kSiteMmaQFull)) return false;
+          ++qc[x];
+        }
+        const int r = rc % R;
+        if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
+        tc_fence_after();
+        const uint32_t qa = sbase + C::kOffQ + x * C::kQTile;
+        const uint32_t ka = sbase + C::kOffRing + r * C::kKVTile;
+        const uint32_t idesc = (nblk == G) ? C::kIdescS : C::kIdescS1;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(tmem + x * C::kSlotCols,
+                    sdesc_sw128(qa + (kk >> 2) * C::kQRegion + (kk & 3) * 32, 16, 1024),
+                    sdesc_sw128(ka + (kk >> 2) * C::kKVRegion + (kk & 3) * 32, 16, 1024), idesc,
+                    kk > 0);
+        tc_commit(bar(C::kBarRE + r));
+        tc_commit(bar(C::kBarSF + x));
+        if (step == (it.w + G - 1) / G - 1) tc_commit(bar(C::kBarQE + x));
+        ++rc;
+        return true;
+      });
 
-  for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
-    const int nnz = p.items[t].w;
-    if (nnz == 0) continue;
-    ok = mbar_wait(bar(C::kBarQF), qc & 1, ctl, kSiteMmaQFull);
-    if (!ok) break;
-    ++qc;
-    tc_fence_after();
-    ok = issue_s();
-    if (!ok) break;
-    if (nnz == 1) tc_commit(bar(C::kBarQE));
-    for (int j = 0; j < nnz; ++j) {
-      if (j + 1 < nnz) {
-        ok = issue_s();
-        if (!ok) break;
-        if (j + 2 == nnz) tc_commit(bar(C::kBarQE));  // last S of the item issued
-      }
-      ok = mbar_wait(bar(C::kBarPF), pc & 1, ctl, kSiteMmaPFull);
-      if (!ok) break;
-      const int vs = vc % S;
-      ok = mbar_wait(bar(C::kBarVF + vs), (vc / S) & 1, ctl, kSiteMmaVFull);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t pa = sbase + C::kOffP;
-      const uint32_t va = sbase + C::kOffV + vs * C::kTile;
-#pragma unroll
-      for (int kk = 0; kk < BLK / 16; ++kk) {
-        const uint32_t aoff = (kk >> 2) * C::kRegion + (kk & 3) * 32;
-        tc_mma_ss(tmem + C::kOCol, sdesc_sw128(pa + aoff, 16, 1024),
-                  sdesc_sw128(va + kk * 16 * 128, C::kRegion, 1024), C::kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      tc_commit(bar(C::kBarVE + vs));
-      tc_commit(bar(C::kBarOF));
-      ++vc;
-      ++pc;
-    }
-  }
   // Let every MMA issued so far finish before TMEM is released.
   tc_commit(bar(C::kBarDrain));
   mbar_drain_wait(bar(C::kBarDrain), 0);
@@ -233,25 +293,68 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
 
 // ------------------------------------------------------------ softmax group
 
+// Loads this thread's NC score columns of the slot's S into x[].
+template <int BLK, int NC>
+__device__ __forceinline__ void load_s(uint32_t ts, float (&x)[NC]) {
+  if constexpr (BLK == 128) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld_32x32b_x32(ts + 0, r0);
+    tmem_ld_32x32b_x32(ts + 32, r1);
+    tmem_ld_32x32b_x32(ts + 64, r2);
+    tmem_ld_32x32b_x32(ts + 96, r3);
+    tmem_ld_wait(r0);
+    tmem_ld_wait(r1);
+    tmem_ld_wait(r2);
+    tmem_ld_wait(r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] = __uint_as_float(r0[i]);
+      x[32 + i] = __uint_as_float(r1[i]);
+      x[64 + i] = __uint_as_float(r2[i]);
+      x[96 + i] = __uint_as_float(r3[i]);
+    }
+  } else {
+    // lanes 0-15 get columns [0, 64) of their row, lanes 16-31 columns [64, 128)
+    uint32_t r0[32], r1[32];
+    tmem_ld_16x32bx2_x32<64>(ts + 0, r0);
+    tmem_ld_16x32bx2_x32<64>(ts + 32, r1);
+    tmem_ld_wait(r0);
+    tmem_ld_wait(r1);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] = __uint_as_float(r0[i]);
+      x[32 + i] = __uint_as_float(r1[i]);
+    }
+  }
+}
+
 template <int BLK, int D>
 __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, uint32_t tmem,
-                                            const WaitCtl& ctl) {
+                                            int slot, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
-  constexpr int NC = (BLK == 128) ? 128 : 32;  // S columns held per thread
+  constexpr int G = C::kG;
+  constexpr int NC = (BLK == 128) ? 128 : 64;   // S columns held per thread
   constexpr int OC = (BLK == 128) ? D : D / 2;  // O columns held per thread
+  constexpr int NA = 8;                         // independent reduction chains
   constexpr float kLn2 = 0.6931471805599453f;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int row = (BLK == 128) ? (wq * 32 + lane) : (wq * 16 + (lane & 15));
-  const int half = (BLK == 128) ? 0 : (lane >> 4);
-  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-  const uint32_t p_tile = sbase + C::kOffP;
+  const int half = (BLK == 128) ? 0 : (lane >> 4);  // which block of the step (b = 64)
+  const uint32_t ts = tmem + (static_cast<uint32_t>(wq * 32) << 16) + slot * C::kSlotCols;
+  const uint32_t to = ts + C::kOCol;
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+  // scale > 0: the row max of the raw scores gives the max of the scaled ones and the
+  // exponent is one FFMA.  Otherwise the scores are scaled first (c = 1 afterwards).
+  const bool pos_scale = p.scale_log2 > 0.f;
+  const float cs = pos_scale ? p.scale_log2 : 1.f;
   int sc = 0, oc = 0;
   bool ok = true;
 
-  for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+  for (int k = slot;; k += 2) {
+    const int t = blockIdx.x + k * gridDim.x;
+    if (t >= p.n_items || !ok) break;
     const int4 it = p.items[t];
     const int nnz = it.w;
     const int qrow = (it.x * p.H + it.y) * p.L + it.z * BLK + row;  // global query row
@@ -262,113 +365,112 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       if (half == 0) p.lse[qrow] = -INFINITY;
       continue;
     }
-    const int start = p.row_ptr[it.y * p.nb + it.z];
+    const int* cols = p.col_idx + p.row_ptr[it.y * p.nb + it.z];
+    const int nsteps = (nnz + G - 1) / G;
     float m_used = -INFINITY;
     float l = 0.f;
-    for (int j = 0; j < nnz; ++j) {
-      const bool diag = p.causal_diag && (p.col_idx[start + j] == it.z);
-      const int sb = sc & 1;
-      ok = mbar_wait(bar(C::kBarSF + sb), (sc >> 1) & 1, ctl, kSiteSoftSFull);
+    for (int s = 0; s < nsteps; ++s) {
+      const int nblk = step_blocks<G>(nnz, s);
+      const bool valid = half < nblk;
+      const bool diag = valid && p.causal_diag && (cols[s * G + half] == it.z);
+      ok = mbar_wait(bar(C::kBarSF + slot), sc & 1, ctl, kSiteSoftSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      ++sc;
       tc_fence_after();
       float x[NC];
-      if constexpr (BLK == 128) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tl + sb * C::kSCols + c * 32, r);
-          tmem_ld_wait(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
-        }
-      } else {
-        uint32_t r[32];
-        tmem_ld_16x32bx2_x32<32>(tl + sb * C::kSCols, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarSE + sb));
-      ++sc;
+      load_s<BLK, NC>(ts, x);
 
-      // scores in log2 units, causal mask inside the diagonal block
-      float mx = -INFINITY;
+      if (!pos_scale) {
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int key = half * 32 + c;
-        float v = x[c] * p.scale_log2;
-        if (diag && key > row) v = -INFINITY;
-        x[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < NC; ++c) x[c] *= p.scale_log2;
       }
+      if (!valid) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
+      } else if (diag) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (c > row) x[c] = -INFINITY;
+      }
+      float mr[NA];
+#pragma unroll
+      for (int a = 0; a < NA; ++a) mr[a] = x[a];
+#pragma unroll
+      for (int c = NA; c < NC; ++c) mr[c % NA] = fmaxf(mr[c % NA], x[c]);
+#pragma unroll
+      for (int w = NA / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int a = 0; a < w; ++a) mr[a] = fmaxf(mr[a], mr[a + w]);
+      float mx = mr[0] * cs;  // -inf stays -inf (cs > 0)
       if constexpr (BLK == 64) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       float alpha = 1.f;
       const float m_new = fmaxf(m_used, mx);
-      if (j == 0) {
+      if (s == 0) {
         m_used = m_new;
       } else if (m_new > m_used + 8.f) {
         alpha = ex2_approx(m_used - m_new);
         m_used = m_new;
       }
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        x[c] = ex2_approx(x[c] - msub);
-        rs += x[c];
-      }
-      if constexpr (BLK == 64) rs += __shfl_xor_sync(0xffffffffu, rs, 16);
-      l = l * alpha + rs;
+      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
 
-      if (j > 0) {
-        // PV(j-1) must be complete before O is rescaled and P is overwritten.
-        ok = mbar_wait(bar(C::kBarOF), oc & 1, ctl, kSiteSoftOFull);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++oc;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      float sr[NA];
 #pragma unroll
-          for (int c = 0; c < OC / 32; ++c) {
-            uint32_t r[32];
-            if constexpr (BLK == 128) {
-              tmem_ld_32x32b_x32(tl + C::kOCol + c * 32, r);
-            } else {
-              tmem_ld_16x32bx2_x32<D / 2>(tl + C::kOCol + c * 32, r);
-            }
-            tmem_ld_wait(r);
+      for (int a = 0; a < NA; ++a) sr[a] = 0.f;
+      // exp2, row sum and P (bf16 pairs) -> TMEM over the S columns, 32 columns at a time.
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            if constexpr (BLK == 128) {
-              tmem_st_32x32b_x32(tl + C::kOCol + c * 32, r);
-            } else {
-              tmem_st_16x32bx2_x32<D / 2>(tl + C::kOCol + c * 32, r);
-            }
-          }
-          tmem_st_wait();
+      for (int cc = 0; cc < NC / 64; ++cc) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e0 = ex2_approx(fmaf(x[cc * 64 + 2 * i], cs, neg_m));
+          const float e1 = ex2_approx(fmaf(x[cc * 64 + 2 * i + 1], cs, neg_m));
+          sr[(2 * i) % NA] += e0;
+          sr[(2 * i + 1) % NA] += e1;
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+        if constexpr (BLK == 128) {
+          tmem_st_32x32b_x32(ts + cc * 32, pk);
+        } else {
+          tmem_st_16x32bx2_x32<32>(ts, pk);
         }
       }
-      // P -> shared memory, bf16, K-major 128-byte-swizzled (8 keys per 16-byte chunk).
 #pragma unroll
-      for (int q = 0; q < NC / 8; ++q) {
-        const int ch = half * 4 + q;  // chunk index along the keys of this row
-        const int region = ch >> 3;
-        const int phys = (ch & 7) ^ (row & 7);
-        const uint32_t addr = p_tile + region * C::kRegion + row * 128 + phys * 16;
-        st_shared_v4(addr, pack_bf16x2(x[8 * q + 0], x[8 * q + 1]),
-                     pack_bf16x2(x[8 * q + 2], x[8 * q + 3]), pack_bf16x2(x[8 * q + 4], x[8 * q + 5]),
-                     pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+      for (int w = NA / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int a = 0; a < w; ++a) sr[a] += sr[a + w];
+      float rs = sr[0];
+      if constexpr (BLK == 64) rs += __shfl_xor_sync(0xffffffffu, rs, 16);
+      l = l * alpha + rs;
+      // O rescale: S(s) complete implies PV(s-1) complete; PV(s) waits for P below.
+      if (s > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < OC / 32; ++c) {
+          uint32_t r[32];
+          if constexpr (BLK == 128) {
+            tmem_ld_32x32b_x32(to + c * 32, r);
+          } else {
+            tmem_ld_16x32bx2_x32<D / 2>(to + c * 32, r);
+          }
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          if constexpr (BLK == 128) {
+            tmem_st_32x32b_x32(to + c * 32, r);
+          } else {
+            tmem_st_16x32bx2_x32<D / 2>(to + c * 32, r);
+          }
+        }
       }
-      fence_proxy_async_smem();
+
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPF));
+      mbar_arrive(bar(C::kBarPF + slot));
     }
     if (!ok) break;
 
-    // epilogue: wait for the last PV, then O / l -> bf16 and lse.
-    ok = mbar_wait(bar(C::kBarOF), oc & 1, ctl, kSiteSoftOFull);
+    // epilogue: wait for the item's last PV, then O / l -> bf16 and lse.
+    ok = mbar_wait(bar(C::kBarOF + slot), oc & 1, ctl, kSiteSoftOFull);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     ++oc;
@@ -378,9 +480,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
     for (int c = 0; c < OC / 32; ++c) {
       uint32_t r[32];
       if constexpr (BLK == 128) {
-        tmem_ld_32x32b_x32(tl + C::kOCol + c * 32, r);
+        tmem_ld_32x32b_x32(to + c * 32, r);
       } else {
-        tmem_ld_16x32bx2_x32<D / 2>(tl + C::kOCol + c * 32, r);
+        tmem_ld_16x32bx2_x32<D / 2>(to + c * 32, r);
       }
       tmem_ld_wait(r);
 #pragma unroll
@@ -400,7 +502,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 // ------------------------------------------------------------------- kernel
 
 template <int BLK, int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<BLK, D>;
@@ -415,21 +517,18 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-    mbar_init(bar(C::kBarQF), 1);
-    mbar_init(bar(C::kBarQE), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKF + s), 1);
-      mbar_init(bar(C::kBarKE + s), 1);
-      mbar_init(bar(C::kBarVF + s), 1);
-      mbar_init(bar(C::kBarVE + s), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::kBarQF + x), 1);
+      mbar_init(bar(C::kBarQE + x), 1);
+      mbar_init(bar(C::kBarSF + x), 1);
+      mbar_init(bar(C::kBarPF + x), 128);
+      mbar_init(bar(C::kBarOF + x), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::kBarSF + s), 1);
-      mbar_init(bar(C::kBarSE + s), 128);
-    }
-    mbar_init(bar(C::kBarPF), 128);
-    mbar_init(bar(C::kBarOF), 1);
     mbar_init(bar(C::kBarDrain), 1);
+    for (int r = 0; r < C::kRing; ++r) {
+      mbar_init(bar(C::kBarRF + r), 1);
+      mbar_init(bar(C::kBarRE + r), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -453,7 +552,7 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1) {
     if (lane == 0) fwd_mma<BLK, D>(p, sbase, tmem, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<BLK, D>(p, sbase, tmem, ctl);
+    fwd_softmax<BLK, D>(p, sbase, tmem, (warp - 4) >> 2, ctl);
   }
 
   tc_fence_before();

@@ -43,13 +43,10 @@ struct FwdParams {
 // Wait-site ids recorded in the status word's low bits.
 enum WaitSite : int {
   kSiteProdQEmpty = 1,
-  kSiteProdKEmpty = 2,
-  kSiteProdVEmpty = 3,
+  kSiteProdRingEmpty = 2,
   kSiteMmaQFull = 4,
-  kSiteMmaSEmpty = 5,
-  kSiteMmaKFull = 6,
+  kSiteMmaRingFull = 6,
   kSiteMmaPFull = 7,
-  kSiteMmaVFull = 8,
   kSiteSoftSFull = 9,
   kSiteSoftOFull = 10,
   kSiteSelftest = 15,

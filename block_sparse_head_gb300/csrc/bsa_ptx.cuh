@@ -113,6 +113,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Prefetch one box of a 2D tiled tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (tcgen05.mma
 // operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
