@@ -238,6 +238,14 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   int qc[2] = {0, 0}, pc[2] = {0, 0};
   int rc = 0;
+  // Descriptors are built once; per MMA only the low word (start address >> 4) moves.
+  const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffRing, 16, 1024);          // K-major
+  const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffRing, C::kKVRegion, 1024);  // MN-major
+  const uint32_t desc_hi = static_cast<uint32_t>(kdesc0 >> 32);  // same for Q, K and V
+  const uint32_t k_lo0 = static_cast<uint32_t>(kdesc0);
+  const uint32_t v_lo0 = static_cast<uint32_t>(vdesc0);
+  const uint32_t q_lo0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffQ, 16, 1024));
+  constexpr uint32_t kTileStep = C::kKVTile >> 4;  // descriptor units per ring tile
 
   walk_schedule<G>(
       p,
@@ -249,13 +257,14 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
         if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
         tc_fence_after();
         const uint32_t ts = tmem + x * C::kSlotCols;
-        const uint32_t va = sbase + C::kOffRing + r * C::kKVTile;
-        const int ksteps = nblk * BLK / 16;
+        const uint32_t vlo = v_lo0 + r * kTileStep;
+        tc_mma_ts_lh(ts + C::kOCol, ts, vlo, desc_hi, C::kIdescPV, step > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < C::kKR / 16; ++kk)
-          if (kk < ksteps)
-            tc_mma_ts(ts + C::kOCol, ts + kk * 8, sdesc_sw128(va + kk * 16 * 128, C::kKVRegion, 1024),
-                      C::kIdescPV, (step > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 1; kk < C::kKR / 16; ++kk) {
+          if (kk < nblk * BLK / 16)
+            tc_mma_ts_lh(ts + C::kOCol, ts + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi,
+                         C::kIdescPV, 1u);
+        }
         tc_commit(bar(C::kBarRE + r));
         if (last) tc_commit(bar(C::kBarOF + x));
         ++rc;
@@ -270,15 +279,15 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
         const int r = rc % R;
         if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + C::kOffQ + x * C::kQTile;
-        const uint32_t ka = sbase + C::kOffRing + r * C::kKVTile;
+        const uint32_t qlo = q_lo0 + x * (C::kQTile >> 4);
+        const uint32_t klo = k_lo0 + r * kTileStep;
         const uint32_t idesc = (nblk == G) ? C::kIdescS : C::kIdescS1;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tmem + x * C::kSlotCols,
-                    sdesc_sw128(qa + (kk >> 2) * C::kQRegion + (kk & 3) * 32, 16, 1024),
-                    sdesc_sw128(ka + (kk >> 2) * C::kKVRegion + (kk & 3) * 32, 16, 1024), idesc,
-                    kk > 0);
+          tc_mma_ss_lh(tmem + x * C::kSlotCols,
+                       qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), desc_hi,
+                       klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), desc_hi, idesc,
+                       kk > 0 ? 1u : 0u);
         tc_commit(bar(C::kBarRE + r));
         tc_commit(bar(C::kBarSF + x));
         if (step == (it.w + G - 1) / G - 1) tc_commit(bar(C::kBarQE + x));
@@ -365,14 +374,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       if (half == 0) p.lse[qrow] = -INFINITY;
       continue;
     }
-    const int* cols = p.col_idx + p.row_ptr[it.y * p.nb + it.z];
+    // Position of the diagonal block inside the row (-1: none, or no causal mask).
+    const int dpos = p.causal_diag ? p.diag_pos[it.y * p.nb + it.z] : -1;
     const int nsteps = (nnz + G - 1) / G;
     float m_used = -INFINITY;
     float l = 0.f;
     for (int s = 0; s < nsteps; ++s) {
       const int nblk = step_blocks<G>(nnz, s);
       const bool valid = half < nblk;
-      const bool diag = valid && p.causal_diag && (cols[s * G + half] == it.z);
+      const bool diag = valid && (s * G + half == dpos);
       ok = mbar_wait(bar(C::kBarSF + slot), sc & 1, ctl, kSiteSoftSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -393,11 +403,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
         for (int c = 0; c < NC; ++c)
           if (c > row) x[c] = -INFINITY;
       }
+      // Row max: NA chains of three-input maxima over columns c = a (mod NA).
       float mr[NA];
 #pragma unroll
-      for (int a = 0; a < NA; ++a) mr[a] = x[a];
+      for (int a = 0; a < NA; ++a) {
+        mr[a] = x[a];
 #pragma unroll
-      for (int c = NA; c < NC; ++c) mr[c % NA] = fmaxf(mr[c % NA], x[c]);
+        for (int c = a + NA; c < NC; c += 2 * NA)
+          mr[a] = (c + NA < NC) ? fmax3(mr[a], x[c], x[c + NA]) : fmaxf(mr[a], x[c]);
+      }
 #pragma unroll
       for (int w = NA / 2; w >= 1; w /= 2)
 #pragma unroll
@@ -414,20 +428,22 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
 
-      float sr[NA];
+      // exp2(x*c - m) on pairs (packed f32x2 FFMA, MUFU ex2).  Row sums in NS packed
+      // accumulators, P (bf16 pairs) -> TMEM over the S columns, 32 columns at a time.
+      constexpr int NS = 4;
+      uint64_t sr2[NS];
 #pragma unroll
-      for (int a = 0; a < NA; ++a) sr[a] = 0.f;
-      // exp2, row sum and P (bf16 pairs) -> TMEM over the S columns, 32 columns at a time.
+      for (int a = 0; a < NS; ++a) sr2[a] = 0ull;
+      const uint64_t c2 = f2_pack(cs, cs), m2 = f2_pack(neg_m, neg_m);
 #pragma unroll
       for (int cc = 0; cc < NC / 64; ++cc) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float e0 = ex2_approx(fmaf(x[cc * 64 + 2 * i], cs, neg_m));
-          const float e1 = ex2_approx(fmaf(x[cc * 64 + 2 * i + 1], cs, neg_m));
-          sr[(2 * i) % NA] += e0;
-          sr[(2 * i + 1) % NA] += e1;
-          pk[i] = pack_bf16x2(e0, e1);
+          const uint64_t y = f2_fma(f2_pack(x[cc * 64 + 2 * i], x[cc * 64 + 2 * i + 1]), c2, m2);
+          const uint64_t e = f2_pack(ex2_approx(f2_lo(y)), ex2_approx(f2_hi(y)));
+          sr2[i % NS] = f2_add(sr2[i % NS], e);
+          pk[i] = pack_bf16x2(f2_lo(e), f2_hi(e));
         }
         if constexpr (BLK == 128) {
           tmem_st_32x32b_x32(ts + cc * 32, pk);
@@ -435,11 +451,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
           tmem_st_16x32bx2_x32<32>(ts, pk);
         }
       }
-#pragma unroll
-      for (int w = NA / 2; w >= 1; w /= 2)
-#pragma unroll
-        for (int a = 0; a < w; ++a) sr[a] += sr[a + w];
-      float rs = sr[0];
+      sr2[0] = f2_add(f2_add(sr2[0], sr2[1]), f2_add(sr2[2], sr2[3]));
+      float rs = f2_lo(sr2[0]) + f2_hi(sr2[0]);
       if constexpr (BLK == 64) rs += __shfl_xor_sync(0xffffffffu, rs, 16);
       l = l * alpha + rs;
       // O rescale: S(s) complete implies PV(s-1) complete; PV(s) waits for P below.

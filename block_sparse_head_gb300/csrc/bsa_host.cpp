@@ -76,7 +76,8 @@ void free_device(bsa_lut* lut) {
   if (lut->d_col_idx) cudaFree(lut->d_col_idx);
   if (lut->d_items) cudaFree(lut->d_items);
   if (lut->d_status) cudaFree(lut->d_status);
-  lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = nullptr;
+  if (lut->d_diag_pos) cudaFree(lut->d_diag_pos);
+  lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = lut->d_diag_pos = nullptr;
   lut->device = -1;
 }
 
@@ -118,6 +119,13 @@ int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bs
       int32_t* dst = lut->col_idx.data() + lut->row_ptr[r];
       for (int j = 0; j < nb; ++j)
         if (lr[j]) *dst++ = j;
+    }
+    // Position of the diagonal block (j == i) inside each row, for the causal mask.
+    lut->diag_pos.assign(rows, -1);
+    for (int r = 0; r < rows; ++r) {
+      const int i = r % nb;
+      for (int e = lut->row_ptr[r]; e < lut->row_ptr[r + 1]; ++e)
+        if (lut->col_idx[e] == i) lut->diag_pos[r] = e - lut->row_ptr[r];
     }
     lut->n_items = static_cast<int>(n_items);
     std::vector<int32_t> raw(static_cast<size_t>(n_items) * 4);
@@ -174,7 +182,8 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
   const size_t nc = std::max<size_t>(lut->col_idx.size(), 1) * 4;
   const size_t ni = lut->items.size() * 4;
   if (cudaMalloc(&lut->d_row_ptr, nr) != cudaSuccess || cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess ||
-      cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess) {
+      cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess ||
+      cudaMalloc(&lut->d_diag_pos, lut->diag_pos.size() * 4) != cudaSuccess) {
     free_device(lut);
     cudaGetLastError();
     return BSA_ERR_ALLOC;
@@ -186,6 +195,8 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
                              cudaMemcpyHostToDevice, st) == cudaSuccess) &&
             cudaMemcpyAsync(lut->d_items, lut->items.data(), ni, cudaMemcpyHostToDevice, st) ==
                 cudaSuccess &&
+            cudaMemcpyAsync(lut->d_diag_pos, lut->diag_pos.data(), lut->diag_pos.size() * 4,
+                            cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
             cudaStreamSynchronize(st) == cudaSuccess;
   if (!ok) {
@@ -230,6 +241,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   p.items = reinterpret_cast<const int4*>(lut->d_items);
   p.row_ptr = lut->d_row_ptr;
   p.col_idx = lut->d_col_idx;
+  p.diag_pos = lut->d_diag_pos;
   p.out = out;
   p.lse = lse;
   p.status = lut->d_status;

@@ -14,11 +14,13 @@ struct bsa_lut {
   std::vector<int32_t> row_ptr;  // [H*nb + 1]
   std::vector<int32_t> col_idx;  // [nnz_total]
   std::vector<int32_t> items;    // [n_items][4] = {b, h, i, nnz}
+  std::vector<int32_t> diag_pos; // [H*nb]: index of block i in row (h, i), or -1
   // device copies (valid after bsa_lut_upload)
   int device = -1;
   int32_t* d_row_ptr = nullptr;
   int32_t* d_col_idx = nullptr;
   int32_t* d_items = nullptr;
+  int32_t* d_diag_pos = nullptr;
   int32_t* d_status = nullptr;
   uint64_t wait_limit_ns = 10000000000ull;
 };
@@ -30,6 +32,7 @@ struct FwdParams {
   const int4* items;        // work list {b, h, i, nnz}
   const int32_t* row_ptr;   // CSR row starts over rows h*nb + i
   const int32_t* col_idx;   // active column blocks, ascending per row
+  const int32_t* diag_pos;  // per row h*nb + i: position of block i in the row, or -1
   void* out;                // bf16 [B,H,L,d]
   float* lse;               // fp32 [B,H,L]
   int32_t* status;          // device status word (0 = fine)

@@ -31,7 +31,7 @@ constexpr size_t kNoAllocScratchWords = kNoAllocScratchBytes / 4;
 // Layout, in int32 words, each part starting on a 16-byte boundary:
 //   [0, 4)           status word (+ padding)
 //   [4, 4 + 4n)      work list, n items of {b, h, i, nnz}
-//   then row_ptr (H*nb + 1 words), then col_idx (nnz words)
+//   then row_ptr (H*nb + 1 words), then diag_pos (H*nb words), then col_idx (nnz words)
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 // Device address of g_noalloc_scratch per device, looked up once with that device
@@ -79,7 +79,8 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
 
   const size_t off_items = 4;
   const size_t off_rowptr = off_items + round4(static_cast<size_t>(lut->n_items) * 4);
-  const size_t off_colidx = off_rowptr + round4(lut->row_ptr.size());
+  const size_t off_diag = off_rowptr + round4(lut->row_ptr.size());
+  const size_t off_colidx = off_diag + round4(lut->diag_pos.size());
   const size_t total = off_colidx + round4(lut->col_idx.size());
   if (total > kNoAllocScratchWords) return BSA_ERR_TOO_LARGE;
 
@@ -108,6 +109,8 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(base + off_rowptr, lut->row_ptr.data(), lut->row_ptr.size() * 4,
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(base + off_diag, lut->diag_pos.data(), lut->diag_pos.size() * 4,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
       (!lut->col_idx.empty() &&
        cudaMemcpyAsync(base + off_colidx, lut->col_idx.data(), lut->col_idx.size() * 4,
                        cudaMemcpyHostToDevice, st) != cudaSuccess))
@@ -117,6 +120,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   p.items = reinterpret_cast<const int4*>(base + off_items);
   p.row_ptr = base + off_rowptr;
   p.col_idx = base + off_colidx;
+  p.diag_pos = base + off_diag;
   p.out = out;
   p.lse = lse;
   p.status = base;

@@ -156,7 +156,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
  *                call synchronizes `stream` after the kernel and returns
  *                BSA_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel gave up.
  *
- * Limit: 4 + 4*n_items + (H*nb + 1) + nnz int32 words (each part rounded up to 4
+ * Limit: 4 + 4*n_items + (H*nb + 1) + H*nb + nnz int32 words (each part rounded up to 4
  * words) must fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before any
  * device work.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any
