@@ -10,30 +10,32 @@
 //
 // Keys are consumed in steps of 128 rows: one block when b = 128, the next two active
 // blocks of the row when b = 64 (the last step of a row with an odd count holds one).
+// A CTA walks its share of the work list as one continuous stream of steps g = 0, 1, ...
 //
-// GB300 mapping.  One CTA per SM, 384 threads, two work items in flight per CTA
-// ("slots" 0 and 1, each with its own Q tile, TMEM S/P and O, and softmax warpgroup),
-// so the tensor core runs one slot's MMAs while the other slot's softmax runs:
-//   warp 0        TMA producer: Q tile of each item into its slot's Q buffer (and an
-//                 L2 prefetch of the slot's next Q), K and V step tiles into one ring
-//                 of kRing slots, in exactly the order the MMA warp consumes them.
-//   warp 1        tcgen05 issuer (one thread) and TMEM owner.  Per slot, alternating:
-//                   O += P V   (M = b, N = d, K = keys; A = P read from TMEM)
-//                   S = Q K^T  (M = b, N = keys, K = d; into the slot's TMEM S, which
-//                              P overwrites in place once the softmax has read S)
-//   warps 4..7    softmax warpgroup of slot 0; warps 8..11 that of slot 1: TMEM ->
-//                 registers, causal mask on diagonal blocks, base-2 online softmax
-//                 (exp2(s*c - m) with c = scale*log2(e) in one FFMA, tree reductions),
-//                 lazy rescale (the running max moves only when it grows by more than
-//                 2^8; O is rescaled in TMEM, which is safe because S(j) completing
-//                 implies PV(j-1) completed), P -> TMEM as bf16, and the epilogue
-//                 (O / l -> bf16, lse = ln 2 * (m + log2 l)); an item with no active
-//                 block writes O = 0 and lse = -inf.
-//   warps 2..3    idle.
-// b = 128 uses M = 128 MMAs (row r of S/P/O in TMEM lane r, one thread per row);
-// b = 64 uses M = 64 MMAs, whose rows sit in lanes 0-15 of each 32-lane quadrant:
-// lanes t and t+16 of a warp share a row, each holding one of the step's two key
-// blocks (16x32bx2 TMEM loads and stores).
+// GB300 mapping.  One CTA per SM, warp-specialised:
+//   warp 0      TMA producer.  Stage t brings K(t) (plus the Q tile when step t opens an
+//               item) and V(t-3) into shared memory and completes one barrier, so the MMA
+//               warp waits once per step for all of its operands.
+//   warp 1      tcgen05 issuer (one thread) and TMEM owner.  TMEM holds three S buffers
+//               and one O accumulator.  Iteration t issues O += P(t-3) V(t-3) and then
+//               S(t) = Q K(t)^T into S[t % 3] (which P(t-3) occupied), so scores run three
+//               steps ahead of the softmax.  The issuing thread is kept free of anything
+//               but its two barrier checks per step: the tensor pipe takes only a couple
+//               of MMAs ahead of issue, so every stall of that thread idles the pipe.
+//   softmax     b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
+//               quadrant, lane t and t+16 holding the two 64-key halves of one row.
+//               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
+//               lane t and t+16 holding the step's two key blocks.  Per step: TMEM ->
+//               registers, causal mask on diagonal blocks, base-2 online softmax (row max
+//               by three-input maxima and one shuffle, exp2(s*c - m) with the scale c =
+//               scale*log2(e) folded into a packed f32x2 FFMA), lazy rescale (the
+//               running max moves only when it grows by more than 2^8), P -> TMEM as bf16
+//               pairs over the S columns.  When an item ends its O is read out while the
+//               next item's first P is handed over, then normalised and stored as bf16
+//               with lse = ln 2 * (m + log2 l).  An item with no active block writes O = 0
+//               and lse = -inf.
+// Work-list records, CSR row starts and column indices are fetched one item / one step
+// ahead of use, so no role waits on a global load in its steady state.
 //
 // Every barrier wait is bounded (WaitCtl): a wait that runs out records a timeout in
 // the status word, and all roles leave their loops, drain in-flight copies and MMAs,
@@ -51,35 +53,34 @@ template <int BLK, int D>
 struct FwdCfg {
   static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-  static constexpr int kThreads = 384;
+  static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // softmax warpgroups
+  static constexpr int kThreads = 128 + 128 * kNumWG;
   static constexpr int kKR = 128;                 // key rows per step
   static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
+  static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
+  static constexpr int kNK = 2;                   // K tiles in shared memory
+  static constexpr int kNV = 3;                   // V tiles in shared memory
   static constexpr int kQTile = BLK * D * 2;      // bytes of one Q tile
   static constexpr int kKVTile = kKR * D * 2;     // bytes of one K or V step tile
   static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
   static constexpr int kKVRegion = kKR * 128;     // one 64-column box of a step tile
-  static constexpr int kSlotCols = 256;           // TMEM columns per slot: S/P then O
-  static constexpr int kOCol = 128;               // O offset inside a slot
+  static constexpr int kOCol = kNS * 128;         // O after the S buffers
   static constexpr int kTmemCols = 512;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = kOffQ + 2 * kQTile;
-  static constexpr int kBarBytes = 512;
-  static constexpr int kRingFit = (232448 - 1024 - kBarBytes - kOffRing) / kKVTile;
-  static constexpr int kRing = kRingFit < 8 ? kRingFit : 8;
-  static constexpr int kOffBar = kOffRing + kRing * kKVTile;
+  static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+  static constexpr int kOffQ = 0;                 // two Q tiles
+  static constexpr int kOffK = kOffQ + 2 * kQTile;
+  static constexpr int kOffV = kOffK + kNK * kKVTile;
+  static constexpr int kOffBar = kOffV + kNV * kKVTile;
   // barrier indices
-  static constexpr int kBarQF = 0;                // [2] per slot
-  static constexpr int kBarQE = 2;                // [2]
-  static constexpr int kBarSF = 4;                // [2]
-  static constexpr int kBarPF = 6;                // [2]
-  static constexpr int kBarOF = 8;                // [2]
-  static constexpr int kBarDrain = 10;
-  static constexpr int kBarRF = 11;               // [kRing] ring full
-  static constexpr int kBarRE = kBarRF + kRing;   // [kRing] ring empty
-  static constexpr int kNumBars = kBarRE + kRing;
-  static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
+  static constexpr int kBarSF = 0;                // [3] S(g) computed
+  static constexpr int kBarPF = 3;                // [3] P(g) in TMEM, O free (one arrive per softmax warp)
+  static constexpr int kBarPVD = 6;               // [3] PV(g) complete
+  static constexpr int kBarKVF = 9;               // [3] stage t landed: K(t) (+Q) and V(t-3)
+  static constexpr int kBarDrain = 12;
+  static constexpr int kNumBars = 13;
+  static constexpr int kBarBytes = 128;           // barriers, TMEM slot, abort flag
+  static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
-  static_assert(kRing >= 4, "ring too small");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // instruction descriptors: S over a full step (N = 128) or a single 64-key block
   static constexpr uint32_t kIdescS = idesc_bf16_f32(BLK, kKR, false, false);
@@ -107,59 +108,79 @@ __device__ __forceinline__ int step_blocks(int nnz, int s) {
   return rem < G ? rem : G;
 }
 
-// Slot X of a CTA owns positions k = X, X+2, X+4, ... of the CTA's round-robin share
-// of the work list (item blockIdx.x + k * gridDim.x).  Advances k to the next
-// non-empty item at or after k; false when the share is exhausted.
-__device__ __forceinline__ bool seek_item(const FwdParams& p, int& k, int4& item) {
-  for (;; k += 2) {
-    const int t = blockIdx.x + k * gridDim.x;
-    if (t >= p.n_items) return false;
-    item = p.items[t];
-    if (item.w > 0) return true;
-  }
-}
+// The CTA's share of the work list (items blockIdx.x + k*gridDim.x, k = 0, 1, ...).
+// Records are fetched two items ahead and each item's CSR row start and diagonal
+// position one item ahead of use.  A record with w = -1 marks the end.
+struct ItemStream {
+  int k;                 // position of the current item in the CTA's share
+  int n;                 // index of the current item among the non-empty ones
+  int4 cur;              // {b, h, i, nnz}
+  int cur_rs, cur_dp;    // first CSR entry of its row, position of block i in it (-1: none)
+  int4 nx1;
+  int nx1_rs, nx1_dp;
+  int4 nx2;
 
-// The consumption schedule shared by the producer and the MMA warp.  Slots take
-// turns; a turn of slot X is: PV of X's pending step (if any), then S of X's next
-// step (the next item's step 0 when the current item is exhausted).  Each action
-// uses one ring tile (V for PV, K for S), so both warps see the same ring order.
-// on_pv(X, item, step, nblk, last_step) / on_s(X, item, step, nblk, k) return false
-// to stop early.
-template <int G, class OnPV, class OnS>
-__device__ __forceinline__ void walk_schedule(const FwdParams& p, OnPV&& on_pv, OnS&& on_s) {
-  int k[2] = {0, 1};
-  int4 it[2];
-  int nsteps[2], s_next[2] = {0, 0}, pend[2] = {-1, -1};
-  bool done[2];
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    done[x] = !seek_item(p, k[x], it[x]);
-    nsteps[x] = done[x] ? 0 : (it[x].w + G - 1) / G;
+  __device__ __forceinline__ static int4 fetch(const FwdParams& p, int k) {
+    const int t = blockIdx.x + k * gridDim.x;
+    return t < p.n_items ? p.items[t] : make_int4(0, 0, 0, -1);
   }
-  while (!(done[0] && done[1])) {
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (done[x]) continue;
-      if (pend[x] >= 0) {
-        if (!on_pv(x, it[x], pend[x], step_blocks<G>(it[x].w, pend[x]), pend[x] == nsteps[x] - 1))
-          return;
-        pend[x] = -1;
-      }
-      if (s_next[x] >= nsteps[x]) {
-        k[x] += 2;
-        if (!seek_item(p, k[x], it[x])) {
-          done[x] = true;
-          continue;
-        }
-        nsteps[x] = (it[x].w + G - 1) / G;
-        s_next[x] = 0;
-      }
-      const int s = s_next[x]++;
-      if (!on_s(x, it[x], s, step_blocks<G>(it[x].w, s), k[x])) return;
-      pend[x] = s;
+  __device__ __forceinline__ static void fetch_aux(const FwdParams& p, const int4& r, int& rs,
+                                                   int& dp) {
+    rs = 0;
+    dp = -1;
+    if (r.w > 0) {
+      const int row = r.y * p.nb + r.z;
+      rs = p.row_ptr[row];
+      dp = p.diag_pos[row];
     }
   }
-}
+  // Moves to the next item (kSkipEmpty: the next one with active blocks).
+  template <bool kSkipEmpty>
+  __device__ __forceinline__ void next(const FwdParams& p) {
+    for (;;) {
+      ++k;
+      cur = nx1;
+      cur_rs = nx1_rs;
+      cur_dp = nx1_dp;
+      nx1 = nx2;
+      fetch_aux(p, nx1, nx1_rs, nx1_dp);
+      nx2 = fetch(p, k + 2);
+      if (cur.w > 0) ++n;
+      if (!kSkipEmpty || cur.w != 0) return;
+    }
+  }
+  template <bool kSkipEmpty>
+  __device__ __forceinline__ void init(const FwdParams& p) {
+    k = -1;
+    n = -1;
+    nx1 = fetch(p, 0);
+    fetch_aux(p, nx1, nx1_rs, nx1_dp);
+    nx2 = fetch(p, 1);
+    next<kSkipEmpty>(p);
+  }
+  __device__ __forceinline__ bool done() const { return cur.w < 0; }
+};
+
+// Steps of the non-empty items, in order.
+template <int G>
+struct StepCursor {
+  ItemStream is;
+  int s, nsteps;
+  __device__ __forceinline__ void init(const FwdParams& p) {
+    is.init<true>(p);
+    s = 0;
+    nsteps = is.done() ? 0 : (is.cur.w + G - 1) / G;
+  }
+  __device__ __forceinline__ void advance(const FwdParams& p) {
+    if (++s >= nsteps) {
+      is.next<true>(p);
+      s = 0;
+      nsteps = is.done() ? 0 : (is.cur.w + G - 1) / G;
+    }
+  }
+  __device__ __forceinline__ bool valid() const { return !is.done(); }
+  __device__ __forceinline__ int nblk() const { return step_blocks<G>(is.cur.w, s); }
+};
 
 // ----------------------------------------------------------------- producer
 
@@ -168,63 +189,105 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
-  constexpr int R = C::kRing;
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  int qc[2] = {0, 0};
-  int rc = 0;
-
-  // Loads the K or V rows of one step into the next ring tile.
-  auto load_step = [&](const CUtensorMap* tm, const int4& it, int step, int nblk) -> bool {
-    const int r = rc % R;
-    if (!mbar_wait(bar(C::kBarRE + r), ((rc / R) & 1) ^ 1, ctl, kSiteProdRingEmpty)) return false;
-    const int rowbase = (it.x * p.H + it.y) * p.L;
-    const int* cols = p.col_idx + p.row_ptr[it.y * p.nb + it.z] + step * G;
-    mbar_arrive_expect_tx(bar(C::kBarRF + r), nblk * BLK * D * 2);
-    for (int g = 0; g < nblk; ++g) {
-      const int krow = rowbase + cols[g] * BLK;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sbase + C::kOffRing + r * C::kKVTile + c * C::kKVRegion + g * BLK * 128, tm,
-                    bar(C::kBarRF + r), c * 64, krow);
-    }
-    ++rc;
-    return true;
+  // Global row of each block of a step (nblk = 0: no step).
+  struct StepRows {
+    int krow[G];
+    int nblk;
   };
 
-  walk_schedule<G>(
-      p,
-      [&](int x, const int4& it, int step, int nblk, bool) { return load_step(tm_v, it, step, nblk); },
-      [&](int x, const int4& it, int step, int nblk, int k) {
-        if (step == 0) {
-          if (!mbar_wait(bar(C::kBarQE + x), (qc[x] & 1) ^ 1, ctl, kSiteProdQEmpty)) return false;
-          mbar_arrive_expect_tx(bar(C::kBarQF + x), C::kQTile);
-          const int qrow = (it.x * p.H + it.y) * p.L + it.z * BLK;
+  StepCursor<G> c;
+  c.init(p);
+  int colv[G];  // column blocks of the cursor's step, loaded one stage ahead
+  auto fetch_cols = [&]() {
+    if (!c.valid()) return;
+    const int nb = c.nblk();
+    const int* cols = p.col_idx + c.is.cur_rs + c.s * G;
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(sbase + C::kOffQ + x * C::kQTile + c * C::kQRegion, tm_q,
-                        bar(C::kBarQF + x), c * 64, qrow);
-          ++qc[x];
-          // Warm L2 with the slot's next Q tile.
-          int k2 = k + 2;
-          int4 nxt;
-          if (seek_item(p, k2, nxt)) {
-            const int nrow = (nxt.x * p.H + nxt.y) * p.L + nxt.z * BLK;
+    for (int g = 0; g < G; ++g) colv[g] = (g < nb) ? cols[g] : 0;
+  };
+  fetch_cols();
+
+  StepRows h1{}, h2{}, h3{};  // steps t-1, t-2, t-3
+  h1.nblk = h2.nblk = h3.nblk = 0;
+  int nsteps = -1;  // known once the cursor runs out
+  int armed = 0;
+  for (int t = 0;; ++t) {
+    StepRows r0{};
+    r0.nblk = 0;
+    bool first = false;
+    int qrow = 0, qb = 0;
+    if (c.valid()) {
+      r0.nblk = c.nblk();
+      const int rowbase = (c.is.cur.x * p.H + c.is.cur.y) * p.L;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(tm_q, c * 64, nrow);
-          }
-        }
-        return load_step(tm_k, it, step, nblk);
-      });
+      for (int g = 0; g < G; ++g) r0.krow[g] = rowbase + colv[g] * BLK;
+      first = (c.s == 0);
+      qrow = rowbase + c.is.cur.z * BLK;
+      qb = c.is.n & 1;
+      if (first && c.is.nx1.w > 0) {
+        // Warm L2 with the following item's Q.
+        const int nrow = (c.is.nx1.x * p.H + c.is.nx1.y) * p.L + c.is.nx1.z * BLK;
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tma_prefetch_l2_2d(tm_q, cc * 64, nrow);
+      }
+      c.advance(p);
+      fetch_cols();  // the next step's columns, consumed one stage later
+    } else {
+      if (nsteps < 0) nsteps = t;
+      if (nsteps == 0 || t >= nsteps + 3) break;
+    }
+    const StepRows rv = h3;
+    // Stage t re-arms the barrier of stage t-3, so the MMA warp must have taken stage t-3;
+    // S(t-3) completing shows that (every stage t < nsteps + 3 follows a step t-3).  A
+    // stage that loads K(t) waits instead for S(t - kNK), which comes later and frees the
+    // K slot; that S also follows the last S of the item two before this one, whose Q
+    // buffer a new item reuses.
+    if ((r0.nblk > 0 && t >= C::kNK) || t >= 3) {
+      const int j = (r0.nblk > 0 && t >= C::kNK) ? t - C::kNK : t - 3;
+      if (!mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
+    }
+    // V slot (t-3) % kNV held V(t-3-kNV): its PV must be complete.
+    if (rv.nblk > 0 && t - 3 >= C::kNV) {
+      const int j = t - 3 - C::kNV;
+      if (!mbar_wait(bar(C::kBarPVD + j % 3), (j / 3) & 1, ctl, kSiteProdVEmpty)) break;
+    }
+    const uint32_t fb = bar(C::kBarKVF + t % 3);
+    const uint32_t bytes = (first ? C::kQTile : 0) + (r0.nblk + rv.nblk) * BLK * D * 2;
+    if (bytes > 0) {
+      mbar_arrive_expect_tx(fb, bytes);
+    } else {
+      mbar_arrive(fb);
+    }
+    ++armed;
+    if (first) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc)
+        tma_load_2d(sbase + C::kOffQ + qb * C::kQTile + cc * C::kQRegion, tm_q, fb, cc * 64, qrow);
+    }
+    const uint32_t kdst = sbase + C::kOffK + (t % C::kNK) * C::kKVTile;
+    for (int g = 0; g < r0.nblk; ++g) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc)
+        tma_load_2d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, cc * 64, r0.krow[g]);
+    }
+    if (rv.nblk > 0) {
+      const uint32_t vdst = sbase + C::kOffV + ((t - 3) % C::kNV) * C::kKVTile;
+      for (int g = 0; g < rv.nblk; ++g) {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc)
+          tma_load_2d(vdst + cc * C::kKVRegion + g * BLK * 128, tm_v, fb, cc * 64, rv.krow[g]);
+      }
+    }
+    h3 = h2;
+    h2 = h1;
+    h1 = r0;
+  }
 
   // Wait until every copy this thread issued has landed (immediate on the normal path).
-  for (int x = 0; x < 2; ++x)
-    if (qc[x] > 0) mbar_drain_wait(bar(C::kBarQF + x), (qc[x] - 1) & 1);
-  for (int r = 0; r < R; ++r)
-    if (rc > r) {
-      const int f = r + R * ((rc - 1 - r) / R);
-      mbar_drain_wait(bar(C::kBarRF + r), (f / R) & 1);
-    }
+  for (int j = (armed > 3 ? armed - 3 : 0); j < armed; ++j)
+    mbar_drain_wait(bar(C::kBarKVF + j % 3), (j / 3) & 1);
 }
 
 // --------------------------------------------------------------- MMA issuer
@@ -233,67 +296,72 @@ template <int BLK, int D>
 __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                         const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
-  constexpr int R = C::kRing;
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  int qc[2] = {0, 0}, pc[2] = {0, 0};
-  int rc = 0;
   // Descriptors are built once; per MMA only the low word (start address >> 4) moves.
-  const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffRing, 16, 1024);          // K-major
-  const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffRing, C::kKVRegion, 1024);  // MN-major
+  const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);              // K-major
+  const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV, C::kKVRegion, 1024);      // MN-major
   const uint32_t desc_hi = static_cast<uint32_t>(kdesc0 >> 32);  // same for Q, K and V
   const uint32_t k_lo0 = static_cast<uint32_t>(kdesc0);
   const uint32_t v_lo0 = static_cast<uint32_t>(vdesc0);
   const uint32_t q_lo0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffQ, 16, 1024));
-  constexpr uint32_t kTileStep = C::kKVTile >> 4;  // descriptor units per ring tile
+  constexpr uint32_t kTileStep = C::kKVTile >> 4;  // descriptor units per K/V tile
 
-  walk_schedule<G>(
-      p,
-      // O_x (+)= P_x V : P from the slot's TMEM S columns, V from the ring.
-      [&](int x, const int4&, int step, int nblk, bool last) -> bool {
-        if (!mbar_wait(bar(C::kBarPF + x), pc[x] & 1, ctl, kSiteMmaPFull)) return false;
-        ++pc[x];
-        const int r = rc % R;
-        if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
-        tc_fence_after();
-        const uint32_t ts = tmem + x * C::kSlotCols;
-        const uint32_t vlo = v_lo0 + r * kTileStep;
-        tc_mma_ts_lh(ts + C::kOCol, ts, vlo, desc_hi, C::kIdescPV, step > 0 ? 1u : 0u);
+  // What an iteration needs of a step (nblk = 0: no step).
+  struct StepInfo {
+    int nblk;
+    int first;  // first step of its item
+    int qb;     // Q buffer of its item
+  };
+  StepCursor<G> c;
+  c.init(p);
+  StepInfo h1{0, 0, 0}, h2{0, 0, 0}, h3{0, 0, 0};  // steps t-1, t-2, t-3
+  int nsteps = -1;
+  for (int t = 0;; ++t) {
+    StepInfo r0{0, 0, 0};
+    if (c.valid()) {
+      r0.nblk = c.nblk();
+      r0.first = (c.s == 0);
+      r0.qb = c.is.n & 1;
+      c.advance(p);
+    } else {
+      if (nsteps < 0) nsteps = t;
+      if (nsteps == 0 || t >= nsteps + 3) break;
+    }
+    const StepInfo pv = h3;
+    // P(t-3) written by the softmax (and, on an item's first step, O read out).
+    if (pv.nblk > 0 &&
+        !mbar_wait(bar(C::kBarPF + (t - 3) % 3), ((t - 3) / 3) & 1, ctl, kSiteMmaPFull))
+      break;
+    if (!mbar_wait(bar(C::kBarKVF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
+    tc_fence_after();
+    const uint32_t sbuf = tmem + (t % 3) * 128;  // P(t-3), then S(t)
+    if (pv.nblk > 0) {
+      const uint32_t od = tmem + C::kOCol;
+      const uint32_t vlo = v_lo0 + ((t - 3) % C::kNV) * kTileStep;
+      const int ksteps = pv.nblk * BLK / 16;
+      tc_mma_ts_lh(od, sbuf, vlo, desc_hi, C::kIdescPV, pv.first ? 0u : 1u);
 #pragma unroll
-        for (int kk = 1; kk < C::kKR / 16; ++kk) {
-          if (kk < nblk * BLK / 16)
-            tc_mma_ts_lh(ts + C::kOCol, ts + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi,
-                         C::kIdescPV, 1u);
-        }
-        tc_commit(bar(C::kBarRE + r));
-        if (last) tc_commit(bar(C::kBarOF + x));
-        ++rc;
-        return true;
-      },
-      // S_x = Q_x K^T into the slot's TMEM S columns.
-      [&](int x, const int4& it, int step, int nblk, int) -> bool {
-        if (step == 0) {
-          if (!mbar_wait(bar(C::kBarQF + x), qc[x] & 1, ctl, kSiteMmaQFull)) return false;
-          ++qc[x];
-        }
-        const int r = rc % R;
-        if (!mbar_wait(bar(C::kBarRF + r), (rc / R) & 1, ctl, kSiteMmaRingFull)) return false;
-        tc_fence_after();
-        const uint32_t qlo = q_lo0 + x * (C::kQTile >> 4);
-        const uint32_t klo = k_lo0 + r * kTileStep;
-        const uint32_t idesc = (nblk == G) ? C::kIdescS : C::kIdescS1;
+      for (int kk = 1; kk < C::kKR / 16; ++kk)
+        if (kk < ksteps)
+          tc_mma_ts_lh(od, sbuf + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
+      tc_commit(bar(C::kBarPVD + (t - 3) % 3));
+    }
+    if (r0.nblk > 0) {
+      const uint32_t qlo = q_lo0 + r0.qb * (C::kQTile >> 4);
+      const uint32_t klo = k_lo0 + (t % C::kNK) * kTileStep;
+      const uint32_t idesc = (r0.nblk == G) ? C::kIdescS : C::kIdescS1;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_lh(tmem + x * C::kSlotCols,
-                       qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), desc_hi,
-                       klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), desc_hi, idesc,
-                       kk > 0 ? 1u : 0u);
-        tc_commit(bar(C::kBarRE + r));
-        tc_commit(bar(C::kBarSF + x));
-        if (step == (it.w + G - 1) / G - 1) tc_commit(bar(C::kBarQE + x));
-        ++rc;
-        return true;
-      });
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma_ss_lh(sbuf, qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), desc_hi,
+                     klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), desc_hi, idesc,
+                     kk > 0 ? 1u : 0u);
+      tc_commit(bar(C::kBarSF + t % 3));
+    }
+    h3 = h2;
+    h2 = h1;
+    h1 = r0;
+  }
 
   // Let every MMA issued so far finish before TMEM is released.
   tc_commit(bar(C::kBarDrain));
@@ -302,95 +370,130 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
 
 // ------------------------------------------------------------ softmax group
 
-// Loads this thread's NC score columns of the slot's S into x[].
-template <int BLK, int NC>
-__device__ __forceinline__ void load_s(uint32_t ts, float (&x)[NC]) {
-  if constexpr (BLK == 128) {
-    uint32_t r0[32], r1[32], r2[32], r3[32];
-    tmem_ld_32x32b_x32(ts + 0, r0);
-    tmem_ld_32x32b_x32(ts + 32, r1);
-    tmem_ld_32x32b_x32(ts + 64, r2);
-    tmem_ld_32x32b_x32(ts + 96, r3);
-    tmem_ld_wait(r0);
-    tmem_ld_wait(r1);
-    tmem_ld_wait(r2);
-    tmem_ld_wait(r3);
+// O columns [c, c+32) of this thread's half row: lanes 0-15 hold columns c.., lanes
+// 16-31 columns D/2 + c.. of the same rows.
+template <int D>
+__device__ __forceinline__ void load_o32(uint32_t to, int c, uint32_t (&r)[32]) {
+  tmem_ld_16x32bx2_x32<D / 2>(to + c, r);
+}
+template <int D>
+__device__ __forceinline__ void store_o32(uint32_t to, int c, const uint32_t (&r)[32]) {
+  tmem_st_16x32bx2_x32<D / 2>(to + c, r);
+}
+
+// Reads this thread's half row of O, scales it by inv and packs it to bf16 pairs.
+template <int D>
+__device__ __forceinline__ void read_o(uint32_t to, float inv, uint32_t (&pk)[D / 4]) {
+  constexpr int OC = D / 2;
+  uint32_t r[OC / 32][32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      x[i] = __uint_as_float(r0[i]);
-      x[32 + i] = __uint_as_float(r1[i]);
-      x[64 + i] = __uint_as_float(r2[i]);
-      x[96 + i] = __uint_as_float(r3[i]);
-    }
-  } else {
-    // lanes 0-15 get columns [0, 64) of their row, lanes 16-31 columns [64, 128)
-    uint32_t r0[32], r1[32];
-    tmem_ld_16x32bx2_x32<64>(ts + 0, r0);
-    tmem_ld_16x32bx2_x32<64>(ts + 32, r1);
-    tmem_ld_wait(r0);
-    tmem_ld_wait(r1);
+  for (int c = 0; c < OC / 32; ++c) load_o32<D>(to, c * 32, r[c]);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      x[i] = __uint_as_float(r0[i]);
-      x[32 + i] = __uint_as_float(r1[i]);
-    }
-  }
+  for (int c = 0; c < OC / 32; ++c) tmem_ld_wait(r[c]);
+#pragma unroll
+  for (int c = 0; c < OC / 32; ++c)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[c * 16 + i] =
+          pack_bf16x2(__uint_as_float(r[c][2 * i]) * inv, __uint_as_float(r[c][2 * i + 1]) * inv);
+}
+
+// Stores a packed half row (16-byte stores) and, from half 0, the lse.
+template <int D>
+__device__ __forceinline__ void store_o(const FwdParams& p, int qrow, int half,
+                                        const uint32_t (&pk)[D / 4], float m, float l) {
+  constexpr int OC = D / 2;
+  constexpr float kLn2 = 0.6931471805599453f;
+  uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                         static_cast<size_t>(qrow) * D + half * OC);
+#pragma unroll
+  for (int q = 0; q < OC / 8; ++q)
+    orow[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  if (half == 0) p.lse[qrow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 template <int BLK, int D>
 __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, uint32_t tmem,
-                                            int slot, const WaitCtl& ctl) {
+                                            const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
   constexpr int G = C::kG;
-  constexpr int NC = (BLK == 128) ? 128 : 64;   // S columns held per thread
-  constexpr int OC = (BLK == 128) ? D : D / 2;  // O columns held per thread
-  constexpr int NA = 8;                         // independent reduction chains
-  constexpr float kLn2 = 0.6931471805599453f;
+  constexpr int NC = 64;      // score columns per thread
+  constexpr int OC = D / 2;   // O columns per thread
+  constexpr int NA = 8;       // independent max chains
+  constexpr int NS = 4;       // packed sum accumulators
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const int wg = (threadIdx.x >> 7) - 1;  // softmax warpgroup
   const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
-  const int row = (BLK == 128) ? (wq * 32 + lane) : (wq * 16 + (lane & 15));
-  const int half = (BLK == 128) ? 0 : (lane >> 4);  // which block of the step (b = 64)
-  const uint32_t ts = tmem + (static_cast<uint32_t>(wq * 32) << 16) + slot * C::kSlotCols;
-  const uint32_t to = ts + C::kOCol;
+  const int half = lane >> 4;
+  // Row of the query block held by this lane pair, and the TMEM lane base of the warp.
+  const int row = (BLK == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
+  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (BLK == 128 ? wg * 16 : 0)) << 16);
+  const uint32_t to = tl + C::kOCol;
+  // b = 128: this half holds keys [64*half, 64*half + 64) of the step's block.
+  // b = 64: this half holds block `half` of the step (all of its 64 keys).
+  const int kbase = (BLK == 128) ? 64 * half : 0;
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
   // scale > 0: the row max of the raw scores gives the max of the scaled ones and the
   // exponent is one FFMA.  Otherwise the scores are scaled first (c = 1 afterwards).
   const bool pos_scale = p.scale_log2 > 0.f;
   const float cs = pos_scale ? p.scale_log2 : 1.f;
-  int sc = 0, oc = 0;
+  int g = 0;
   bool ok = true;
+  bool have_pending = false;
+  int pend_row = 0;
+  float pend_m = 0.f, pend_l = 0.f;
 
-  for (int k = slot;; k += 2) {
-    const int t = blockIdx.x + k * gridDim.x;
-    if (t >= p.n_items || !ok) break;
-    const int4 it = p.items[t];
+  // Every thread of a warp has finished its TMEM traffic: one arrive per warp.
+  auto warp_arrive = [&](int b) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(b));
+  };
+  // Waits (bounded, warp-uniform result) for phase `parity` of barrier b.
+  auto wait_bar = [&](int b, int parity, int site) -> bool {
+    bool w = mbar_wait(bar(b), parity, ctl, site);
+    w = __all_sync(0xffffffffu, w);
+    if (w) tc_fence_after();
+    return w;
+  };
+
+  ItemStream is;
+  for (is.init<false>(p); ok && !is.done(); is.next<false>(p)) {
+    const int4 it = is.cur;
     const int nnz = it.w;
     const int qrow = (it.x * p.H + it.y) * p.L + it.z * BLK + row;  // global query row
-    uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
     if (nnz == 0) {
+      uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
 #pragma unroll
       for (int c = 0; c < OC / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
       if (half == 0) p.lse[qrow] = -INFINITY;
       continue;
     }
-    // Position of the diagonal block inside the row (-1: none, or no causal mask).
-    const int dpos = p.causal_diag ? p.diag_pos[it.y * p.nb + it.z] : -1;
+    const int dpos = p.causal_diag ? is.cur_dp : -1;  // position of block i in the row
     const int nsteps = (nnz + G - 1) / G;
     float m_used = -INFINITY;
     float l = 0.f;
-    for (int s = 0; s < nsteps; ++s) {
+    for (int s = 0; s < nsteps; ++s, ++g) {
       const int nblk = step_blocks<G>(nnz, s);
-      const bool valid = half < nblk;
-      const bool diag = valid && (s * G + half == dpos);
-      ok = mbar_wait(bar(C::kBarSF + slot), sc & 1, ctl, kSiteSoftSFull);
-      ok = __all_sync(0xffffffffu, ok);
+      const bool valid = (BLK == 128) || (half < nblk);
+      const bool diag = valid && (((BLK == 128) ? s : s * 2 + half) == dpos);
+      const uint32_t ts = tl + (g % 3) * 128;
+      ok = wait_bar(C::kBarSF + g % 3, (g / 3) & 1, kSiteSoftSFull);
       if (!ok) break;
-      ++sc;
-      tc_fence_after();
       float x[NC];
-      load_s<BLK, NC>(ts, x);
-
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld_16x32bx2_x32<64>(ts + 0, r0);
+        tmem_ld_16x32bx2_x32<64>(ts + 32, r1);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(r0[i]);
+          x[32 + i] = __uint_as_float(r1[i]);
+        }
+      }
       if (!pos_scale) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) x[c] *= p.scale_log2;
@@ -399,11 +502,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 #pragma unroll
         for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
       } else if (diag) {
+        const int qin = row - kbase;  // key c is masked when kbase + c > row (row < BLK)
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          if (c > row) x[c] = -INFINITY;
+          if (c > qin) x[c] = -INFINITY;
       }
-      // Row max: NA chains of three-input maxima over columns c = a (mod NA).
+      // Row max: NA chains of three-input maxima over columns c = a (mod NA), then the
+      // other half of the row (lane ^ 16).
       float mr[NA];
 #pragma unroll
       for (int a = 0; a < NA; ++a) {
@@ -417,7 +522,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 #pragma unroll
         for (int a = 0; a < w; ++a) mr[a] = fmaxf(mr[a], mr[a + w]);
       float mx = mr[0] * cs;  // -inf stays -inf (cs > 0)
-      if constexpr (BLK == 64) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       float alpha = 1.f;
       const float m_new = fmaxf(m_used, mx);
       if (s == 0) {
@@ -428,94 +533,76 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       }
       const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
 
-      // exp2(x*c - m) on pairs (packed f32x2 FFMA, MUFU ex2).  Row sums in NS packed
-      // accumulators, P (bf16 pairs) -> TMEM over the S columns, 32 columns at a time.
-      constexpr int NS = 4;
+      // exp2(x*c - m) on pairs (packed f32x2 FFMA, MUFU ex2); packed row sums; P (bf16
+      // pairs) written over the S columns just read.
       uint64_t sr2[NS];
 #pragma unroll
       for (int a = 0; a < NS; ++a) sr2[a] = 0ull;
       const uint64_t c2 = f2_pack(cs, cs), m2 = f2_pack(neg_m, neg_m);
-#pragma unroll
-      for (int cc = 0; cc < NC / 64; ++cc) {
+      {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const uint64_t y = f2_fma(f2_pack(x[cc * 64 + 2 * i], x[cc * 64 + 2 * i + 1]), c2, m2);
+          const uint64_t y = f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), c2, m2);
           const uint64_t e = f2_pack(ex2_approx(f2_lo(y)), ex2_approx(f2_hi(y)));
           sr2[i % NS] = f2_add(sr2[i % NS], e);
           pk[i] = pack_bf16x2(f2_lo(e), f2_hi(e));
         }
-        if constexpr (BLK == 128) {
-          tmem_st_32x32b_x32(ts + cc * 32, pk);
-        } else {
-          tmem_st_16x32bx2_x32<32>(ts, pk);
-        }
+        tmem_st_16x32bx2_x32<32>(ts, pk);
       }
       sr2[0] = f2_add(f2_add(sr2[0], sr2[1]), f2_add(sr2[2], sr2[3]));
       float rs = f2_lo(sr2[0]) + f2_hi(sr2[0]);
-      if constexpr (BLK == 64) rs += __shfl_xor_sync(0xffffffffu, rs, 16);
+      rs += __shfl_xor_sync(0xffffffffu, rs, 16);
       l = l * alpha + rs;
-      // O rescale: S(s) complete implies PV(s-1) complete; PV(s) waits for P below.
+
+      // O rescale (rare): PV(g-1) must be complete first.  Its barrier cannot have moved
+      // on to PV(g+2), which needs this step's P.
       if (s > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        ok = wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftPvDone);
+        if (!ok) break;
 #pragma unroll
         for (int c = 0; c < OC / 32; ++c) {
           uint32_t r[32];
-          if constexpr (BLK == 128) {
-            tmem_ld_32x32b_x32(to + c * 32, r);
-          } else {
-            tmem_ld_16x32bx2_x32<D / 2>(to + c * 32, r);
-          }
+          load_o32<D>(to, c * 32, r);
           tmem_ld_wait(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          if constexpr (BLK == 128) {
-            tmem_st_32x32b_x32(to + c * 32, r);
-          } else {
-            tmem_st_16x32bx2_x32<D / 2>(to + c * 32, r);
-          }
+          store_o32<D>(to, c * 32, r);
         }
       }
-
+      // First step of an item: the previous item's O (its last PV is g-1) is read out
+      // before this P is handed over, since the next PV overwrites O.
+      uint32_t opk[D / 4];
+      if (s == 0 && have_pending) {
+        ok = wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone);
+        if (!ok) break;
+        read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
+      }
       tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPF + slot));
-    }
-    if (!ok) break;
-
-    // epilogue: wait for the item's last PV, then O / l -> bf16 and lse.
-    ok = mbar_wait(bar(C::kBarOF + slot), oc & 1, ctl, kSiteSoftOFull);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    ++oc;
-    tc_fence_after();
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-    for (int c = 0; c < OC / 32; ++c) {
-      uint32_t r[32];
-      if constexpr (BLK == 128) {
-        tmem_ld_32x32b_x32(to + c * 32, r);
-      } else {
-        tmem_ld_16x32bx2_x32<D / 2>(to + c * 32, r);
-      }
-      tmem_ld_wait(r);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        orow[c * 4 + q] = make_uint4(
-            pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv),
-            pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv),
-            pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv),
-            pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
+      warp_arrive(C::kBarPF + g % 3);
+      if (s == 0 && have_pending) {
+        store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
+        have_pending = false;
       }
     }
-    if (half == 0) p.lse[qrow] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-    tc_fence_before();
+    if (!ok) break;
+    pend_row = qrow;
+    pend_m = m_used;
+    pend_l = l;
+    have_pending = true;
+  }
+  if (ok && have_pending &&
+      wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone)) {
+    uint32_t opk[D / 4];
+    read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
+    store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
   }
 }
 
 // ------------------------------------------------------------------- kernel
 
 template <int BLK, int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<BLK, D>;
@@ -530,18 +617,13 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::kBarQF + x), 1);
-      mbar_init(bar(C::kBarQE + x), 1);
+    for (int x = 0; x < 3; ++x) {
       mbar_init(bar(C::kBarSF + x), 1);
-      mbar_init(bar(C::kBarPF + x), 128);
-      mbar_init(bar(C::kBarOF + x), 1);
+      mbar_init(bar(C::kBarPF + x), 4 * C::kNumWG);
+      mbar_init(bar(C::kBarPVD + x), 1);
+      mbar_init(bar(C::kBarKVF + x), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
-    for (int r = 0; r < C::kRing; ++r) {
-      mbar_init(bar(C::kBarRF + r), 1);
-      mbar_init(bar(C::kBarRE + r), 1);
-    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -565,7 +647,7 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     if (lane == 0) fwd_mma<BLK, D>(p, sbase, tmem, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<BLK, D>(p, sbase, tmem, (warp - 4) >> 2, ctl);
+    fwd_softmax<BLK, D>(p, sbase, tmem, ctl);
   }
 
   tc_fence_before();

@@ -45,13 +45,13 @@ struct FwdParams {
 
 // Wait-site ids recorded in the status word's low bits.
 enum WaitSite : int {
-  kSiteProdQEmpty = 1,
-  kSiteProdRingEmpty = 2,
-  kSiteMmaQFull = 4,
-  kSiteMmaRingFull = 6,
+  kSiteProdKEmpty = 1,
+  kSiteProdVEmpty = 2,
   kSiteMmaPFull = 7,
+  kSiteMmaStage = 6,
   kSiteSoftSFull = 9,
-  kSiteSoftOFull = 10,
+  kSiteSoftPvDone = 11,
+  kSiteSoftItemDone = 12,
   kSiteSelftest = 15,
 };
 
