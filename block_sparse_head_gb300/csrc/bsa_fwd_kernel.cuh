@@ -14,14 +14,16 @@
 //
 // GB300 mapping.  One CTA per SM, warp-specialised:
 //   warp 0      TMA producer.  Stage t brings K(t) (plus the Q tile when step t opens an
-//               item) and V(t-3) into shared memory and completes one barrier, so the MMA
+//               item) and V(t-2) into shared memory and completes one barrier, so the MMA
 //               warp waits once per step for all of its operands.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.  TMEM holds three S buffers
-//               and one O accumulator.  Iteration t issues O += P(t-3) V(t-3) and then
-//               S(t) = Q K(t)^T into S[t % 3] (which P(t-3) occupied), so scores run three
-//               steps ahead of the softmax.  The issuing thread is kept free of anything
-//               but its two barrier checks per step: the tensor pipe takes only a couple
-//               of MMAs ahead of issue, so every stall of that thread idles the pipe.
+//               and one O accumulator.  Iteration t issues S(t) = Q K(t)^T into S[t % 3]
+//               (which P(t-3) occupied; its PV went out in the previous iteration), then
+//               O += P(t-2) V(t-2), so scores run two to three steps ahead of the softmax
+//               and an item's last PV follows its P by about one iteration.  The issuing
+//               thread is kept free of anything but two barrier checks per step, each
+//               placed right after a group of MMAs: the tensor pipe takes only a couple of
+//               MMAs ahead of issue, so every stall of that thread idles the pipe.
 //   softmax     b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
 //               quadrant, lane t and t+16 holding the two 64-key halves of one row.
 //               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
@@ -54,28 +56,30 @@ struct FwdCfg {
   static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // softmax warpgroups
-  static constexpr int kThreads = 128 + 128 * kNumWG;
+  static constexpr int kThreads = 64 + 128 * kNumWG;  // producer warp, MMA warp, softmax
   static constexpr int kKR = 128;                 // key rows per step
   static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
   static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
-  static constexpr int kNK = 2;                   // K tiles in shared memory
+  static constexpr int kNK = 3;                   // K tiles in shared memory
   static constexpr int kNV = 3;                   // V tiles in shared memory
   static constexpr int kQTile = BLK * D * 2;      // bytes of one Q tile
   static constexpr int kKVTile = kKR * D * 2;     // bytes of one K or V step tile
+  // Q tiles: two when they fit beside the K/V tiles, else one (b = 128, d = 128).
+  static constexpr int kNQ = (2 * kQTile + (kNK + kNV) * kKVTile + 1152 <= 232448) ? 2 : 1;
   static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
   static constexpr int kKVRegion = kKR * 128;     // one 64-column box of a step tile
   static constexpr int kOCol = kNS * 128;         // O after the S buffers
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
-  static constexpr int kOffQ = 0;                 // two Q tiles
-  static constexpr int kOffK = kOffQ + 2 * kQTile;
+  static constexpr int kOffQ = 0;                 // kNQ Q tiles
+  static constexpr int kOffK = kOffQ + kNQ * kQTile;
   static constexpr int kOffV = kOffK + kNK * kKVTile;
   static constexpr int kOffBar = kOffV + kNV * kKVTile;
   // barrier indices
   static constexpr int kBarSF = 0;                // [3] S(g) computed
   static constexpr int kBarPF = 3;                // [3] P(g) in TMEM, O free (one arrive per softmax warp)
   static constexpr int kBarPVD = 6;               // [3] PV(g) complete
-  static constexpr int kBarKVF = 9;               // [3] stage t landed: K(t) (+Q) and V(t-3)
+  static constexpr int kBarKVF = 9;               // [3] stage t landed: K(t) (+Q) and V(t-2)
   static constexpr int kBarDrain = 12;
   static constexpr int kNumBars = 13;
   static constexpr int kBarBytes = 128;           // barriers, TMEM slot, abort flag
@@ -209,8 +213,8 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
   };
   fetch_cols();
 
-  StepRows h1{}, h2{}, h3{};  // steps t-1, t-2, t-3
-  h1.nblk = h2.nblk = h3.nblk = 0;
+  StepRows h1{}, h2{};  // steps t-1, t-2
+  h1.nblk = h2.nblk = 0;
   int nsteps = -1;  // known once the cursor runs out
   int armed = 0;
   for (int t = 0;; ++t) {
@@ -225,7 +229,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       for (int g = 0; g < G; ++g) r0.krow[g] = rowbase + colv[g] * BLK;
       first = (c.s == 0);
       qrow = rowbase + c.is.cur.z * BLK;
-      qb = c.is.n & 1;
+      qb = c.is.n % C::kNQ;
       if (first && c.is.nx1.w > 0) {
         // Warm L2 with the following item's Q.
         const int nrow = (c.is.nx1.x * p.H + c.is.nx1.y) * p.L + c.is.nx1.z * BLK;
@@ -236,21 +240,24 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       fetch_cols();  // the next step's columns, consumed one stage later
     } else {
       if (nsteps < 0) nsteps = t;
-      if (nsteps == 0 || t >= nsteps + 3) break;
+      if (nsteps == 0 || t >= nsteps + 2) break;
     }
-    const StepRows rv = h3;
+    const StepRows rv = h2;
     // Stage t re-arms the barrier of stage t-3, so the MMA warp must have taken stage t-3;
-    // S(t-3) completing shows that (every stage t < nsteps + 3 follows a step t-3).  A
-    // stage that loads K(t) waits instead for S(t - kNK), which comes later and frees the
-    // K slot; that S also follows the last S of the item two before this one, whose Q
-    // buffer a new item reuses.
-    if ((r0.nblk > 0 && t >= C::kNK) || t >= 3) {
-      const int j = (r0.nblk > 0 && t >= C::kNK) ? t - C::kNK : t - 3;
-      if (!mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
+    // S(t-3) completing shows that (every stage t < nsteps + 2 follows a step t-3), and
+    // it also frees K slot t % 3 (kNK = 3).  A stage that opens an item needs its Q
+    // buffer back: with one Q buffer the previous item's last S, S(t-1), must be
+    // complete; with two, the last S of the item before that, which is S(t-2) or earlier.
+    // S completes in issue order, so one wait covers all of it.
+    static_assert(C::kNK == 3, "K slot reuse is tied to the three S buffers");
+    {
+      int j = (t >= 3) ? t - 3 : -1;
+      if (first) j = max(j, t - (C::kNQ == 1 ? 1 : 2));
+      if (j >= 0 && !mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
     }
-    // V slot (t-3) % kNV held V(t-3-kNV): its PV must be complete.
-    if (rv.nblk > 0 && t - 3 >= C::kNV) {
-      const int j = t - 3 - C::kNV;
+    // V slot (t-2) % kNV held V(t-2-kNV): its PV must be complete.
+    if (rv.nblk > 0 && t - 2 >= C::kNV) {
+      const int j = t - 2 - C::kNV;
       if (!mbar_wait(bar(C::kBarPVD + j % 3), (j / 3) & 1, ctl, kSiteProdVEmpty)) break;
     }
     const uint32_t fb = bar(C::kBarKVF + t % 3);
@@ -273,14 +280,13 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
         tma_load_2d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, cc * 64, r0.krow[g]);
     }
     if (rv.nblk > 0) {
-      const uint32_t vdst = sbase + C::kOffV + ((t - 3) % C::kNV) * C::kKVTile;
+      const uint32_t vdst = sbase + C::kOffV + ((t - 2) % C::kNV) * C::kKVTile;
       for (int g = 0; g < rv.nblk; ++g) {
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
           tma_load_2d(vdst + cc * C::kKVRegion + g * BLK * 128, tm_v, fb, cc * 64, rv.krow[g]);
       }
     }
-    h3 = h2;
     h2 = h1;
     h1 = r0;
   }
@@ -315,39 +321,29 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
   };
   StepCursor<G> c;
   c.init(p);
-  StepInfo h1{0, 0, 0}, h2{0, 0, 0}, h3{0, 0, 0};  // steps t-1, t-2, t-3
-  int nsteps = -1;
-  for (int t = 0;; ++t) {
+  StepInfo h1{0, 0, 0}, h2{0, 0, 0};  // steps t-1, t-2
+  int nsteps = -1;  // known once the cursor runs out
+  bool ok = true;
+  if (c.valid()) {
+    ok = mbar_wait(bar(C::kBarKVF), 0, ctl, kSiteMmaStage);
+  } else {
+    nsteps = 0;
+  }
+  for (int t = 0; ok && nsteps != 0; ++t) {
     StepInfo r0{0, 0, 0};
     if (c.valid()) {
       r0.nblk = c.nblk();
       r0.first = (c.s == 0);
-      r0.qb = c.is.n & 1;
+      r0.qb = c.is.n % C::kNQ;
       c.advance(p);
-    } else {
-      if (nsteps < 0) nsteps = t;
-      if (nsteps == 0 || t >= nsteps + 3) break;
+      if (!c.valid()) nsteps = t + 1;
     }
-    const StepInfo pv = h3;
-    // P(t-3) written by the softmax (and, on an item's first step, O read out).
-    if (pv.nblk > 0 &&
-        !mbar_wait(bar(C::kBarPF + (t - 3) % 3), ((t - 3) / 3) & 1, ctl, kSiteMmaPFull))
-      break;
-    if (!mbar_wait(bar(C::kBarKVF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
+    if (nsteps >= 0 && t >= nsteps + 2) break;
+    const StepInfo pv = h2;
+    // Stage t has landed (checked at the end of the previous iteration).
     tc_fence_after();
-    const uint32_t sbuf = tmem + (t % 3) * 128;  // P(t-3), then S(t)
-    if (pv.nblk > 0) {
-      const uint32_t od = tmem + C::kOCol;
-      const uint32_t vlo = v_lo0 + ((t - 3) % C::kNV) * kTileStep;
-      const int ksteps = pv.nblk * BLK / 16;
-      tc_mma_ts_lh(od, sbuf, vlo, desc_hi, C::kIdescPV, pv.first ? 0u : 1u);
-#pragma unroll
-      for (int kk = 1; kk < C::kKR / 16; ++kk)
-        if (kk < ksteps)
-          tc_mma_ts_lh(od, sbuf + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
-      tc_commit(bar(C::kBarPVD + (t - 3) % 3));
-    }
     if (r0.nblk > 0) {
+      const uint32_t sbuf = tmem + (t % 3) * 128;
       const uint32_t qlo = q_lo0 + r0.qb * (C::kQTile >> 4);
       const uint32_t klo = k_lo0 + (t % C::kNK) * kTileStep;
       const uint32_t idesc = (r0.nblk == G) ? C::kIdescS : C::kIdescS1;
@@ -358,9 +354,28 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
                      kk > 0 ? 1u : 0u);
       tc_commit(bar(C::kBarSF + t % 3));
     }
-    h3 = h2;
+    if (pv.nblk > 0) {
+      // P(t-2) written by the softmax (and, on an item's first step, O read out).
+      if (!mbar_wait(bar(C::kBarPF + (t - 2) % 3), ((t - 2) / 3) & 1, ctl, kSiteMmaPFull)) break;
+      tc_fence_after();
+      const uint32_t ps = tmem + ((t - 2) % 3) * 128;
+      const uint32_t od = tmem + C::kOCol;
+      const uint32_t vlo = v_lo0 + ((t - 2) % C::kNV) * kTileStep;
+      const int ksteps = pv.nblk * BLK / 16;
+      tc_mma_ts_lh(od, ps, vlo, desc_hi, C::kIdescPV, pv.first ? 0u : 1u);
+#pragma unroll
+      for (int kk = 1; kk < C::kKR / 16; ++kk)
+        if (kk < ksteps)
+          tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
+      tc_commit(bar(C::kBarPVD + (t - 2) % 3));
+    }
     h2 = h1;
     h1 = r0;
+    // Stage t+1, checked while the MMAs just issued are still queued.
+    const int tn = t + 1;
+    if ((nsteps < 0 || tn < nsteps + 2) &&
+        !mbar_wait(bar(C::kBarKVF + tn % 3), (tn / 3) & 1, ctl, kSiteMmaStage))
+      break;
   }
 
   // Let every MMA issued so far finish before TMEM is released.
@@ -422,8 +437,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   constexpr int NA = 8;       // independent max chains
   constexpr int NS = 4;       // packed sum accumulators
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  const int wg = (threadIdx.x >> 7) - 1;  // softmax warpgroup
-  const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
+  const int wg = ((threadIdx.x >> 5) - 2) >> 2;  // softmax group (warps 2-5, 6-9)
+  const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   // Row of the query block held by this lane pair, and the TMEM lane base of the warp.
@@ -646,7 +661,7 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
     if (lane == 0) fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
   } else if (warp == 1) {
     if (lane == 0) fwd_mma<BLK, D>(p, sbase, tmem, ctl);
-  } else if (warp >= 4) {
+  } else {
     fwd_softmax<BLK, D>(p, sbase, tmem, ctl);
   }
 

@@ -94,9 +94,15 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// The common case (the phase completes within a few microseconds) stays inline and never
+// reads the global timer: a handoff through the timed path costs about twice the round
+// trip of a plain spin.  Only a wait that outlasts the spin enters the timed path.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
                                           int site) {
   if (mbar_test_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, ctl, site);
 }
 
