@@ -342,7 +342,7 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
     const StepInfo pv = h2;
     // Stage t has landed (checked at the end of the previous iteration).
     tc_fence_after();
-    if (r0.nblk > 0) {
+    auto issue_s = [&]() {
       const uint32_t sbuf = tmem + (t % 3) * 128;
       const uint32_t qlo = q_lo0 + r0.qb * (C::kQTile >> 4);
       const uint32_t klo = k_lo0 + (t % C::kNK) * kTileStep;
@@ -353,10 +353,11 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
                      klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), desc_hi, idesc,
                      kk > 0 ? 1u : 0u);
       tc_commit(bar(C::kBarSF + t % 3));
-    }
-    if (pv.nblk > 0) {
-      // P(t-2) written by the softmax (and, on an item's first step, O read out).
-      if (!mbar_wait(bar(C::kBarPF + (t - 2) % 3), ((t - 2) / 3) & 1, ctl, kSiteMmaPFull)) break;
+    };
+    // P(t-2) written by the softmax (and, on an item's first step, O read out).
+    auto issue_pv = [&]() -> bool {
+      if (!mbar_wait(bar(C::kBarPF + (t - 2) % 3), ((t - 2) / 3) & 1, ctl, kSiteMmaPFull))
+        return false;
       tc_fence_after();
       const uint32_t ps = tmem + ((t - 2) % 3) * 128;
       const uint32_t od = tmem + C::kOCol;
@@ -368,7 +369,12 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
         if (kk < ksteps)
           tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
       tc_commit(bar(C::kBarPVD + (t - 2) % 3));
-    }
+      return true;
+    };
+    // S(t) first, so the scores keep their lead.  (Issuing an item's last PV first shortens
+    // the softmax's wait at the item boundary, but measured slower on long rows.)
+    if (r0.nblk > 0) issue_s();
+    if (pv.nblk > 0 && !issue_pv()) break;
     h2 = h1;
     h1 = r0;
     // Stage t+1, checked while the MMAs just issued are still queued.
@@ -413,17 +419,25 @@ __device__ __forceinline__ void read_o(uint32_t to, float inv, uint32_t (&pk)[D 
           pack_bf16x2(__uint_as_float(r[c][2 * i]) * inv, __uint_as_float(r[c][2 * i + 1]) * inv);
 }
 
-// Stores a packed half row (16-byte stores) and, from half 0, the lse.
+// Stores a packed half row and, from half 0, the lse.  32-byte stores (whole sectors) when
+// the output base allows it, else 16-byte ones.
 template <int D>
 __device__ __forceinline__ void store_o(const FwdParams& p, int qrow, int half,
                                         const uint32_t (&pk)[D / 4], float m, float l) {
   constexpr int OC = D / 2;
   constexpr float kLn2 = 0.6931471805599453f;
-  uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                         static_cast<size_t>(qrow) * D + half * OC);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(qrow) * D + half * OC;
+  if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
 #pragma unroll
-  for (int q = 0; q < OC / 8; ++q)
-    orow[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    for (int q = 0; q < OC / 16; ++q)
+      st_global_v8(dst + 16 * q, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
+                   pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+  } else {
+    uint4* orow = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < OC / 8; ++q)
+      orow[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
   if (half == 0) p.lse[qrow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
@@ -517,10 +531,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 #pragma unroll
         for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
       } else if (diag) {
-        const int qin = row - kbase;  // key c is masked when kbase + c > row (row < BLK)
+        // Key kbase + c is masked when it lies after the query row.  Predicated selects:
+        // written as branches, the per-lane bounds made this step twice as slow.
+        const int qin = row - kbase;
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (c > qin) x[c] = -INFINITY;
+        for (int c = 0; c < NC; ++c) x[c] = mask_gt(x[c], c, qin);
       }
       // Row max: NA chains of three-input maxima over columns c = a (mod NA), then the
       // other half of the row (lane ^ 16).

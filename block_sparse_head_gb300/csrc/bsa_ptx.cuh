@@ -321,6 +321,26 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 
 
+// x if k <= lim, else -inf, as one predicated select (no branch).
+__device__ __forceinline__ float mask_gt(float x, int k, int lim) {
+  float r;
+  asm("{\n\t.reg .pred p;\n\t"
+      "setp.gt.s32 p, %2, %3;\n\t"
+      "selp.f32 %0, 0fFF800000, %1, p;\n\t}"
+      : "=f"(r)
+      : "f"(x), "r"(k), "r"(lim));
+  return r;
+}
+
+// 32-byte global store (eight 32-bit words); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a0), "r"(a1),
+               "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {
