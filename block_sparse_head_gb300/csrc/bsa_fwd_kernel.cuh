@@ -14,16 +14,15 @@
 //
 // GB300 mapping.  One CTA per SM, warp-specialised:
 //   warp 0      TMA producer.  Stage t brings K(t) (plus the Q tile when step t opens an
-//               item) and V(t-2) into shared memory and completes one barrier, so the MMA
-//               warp waits once per step for all of its operands.
+//               item) and V(t-2) into shared memory.  Its barrier also takes one arrive
+//               per softmax warp for P(t-2), so the MMA warp waits once per step, for
+//               its operands and the softmax's P together.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.  TMEM holds three S buffers
 //               and one O accumulator.  Iteration t issues S(t) = Q K(t)^T into S[t % 3]
 //               (which P(t-3) occupied; its PV went out in the previous iteration), then
-//               O += P(t-2) V(t-2), so scores run two to three steps ahead of the softmax
-//               and an item's last PV follows its P by about one iteration.  The issuing
-//               thread is kept free of anything but two barrier checks per step, each
-//               placed right after a group of MMAs: the tensor pipe takes only a couple of
-//               MMAs ahead of issue, so every stall of that thread idles the pipe.
+//               O += P(t-2) V(t-2): sixteen MMAs back to back, then one barrier check for
+//               the next iteration.  The tensor pipe takes only a couple of MMAs ahead of
+//               issue, so every check or stall of the issuing thread idles the pipe.
 //   softmax     b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
 //               quadrant, lane t and t+16 holding the two 64-key halves of one row.
 //               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
@@ -77,11 +76,10 @@ struct FwdCfg {
   static constexpr int kOffBar = kOffV + kNV * kKVTile;
   // barrier indices
   static constexpr int kBarSF = 0;                // [3] S(g) computed
-  static constexpr int kBarPF = 3;                // [3] P(g) in TMEM, O free (one arrive per softmax warp)
-  static constexpr int kBarPVD = 6;               // [3] PV(g) complete
-  static constexpr int kBarKVF = 9;               // [3] stage t landed: K(t) (+Q) and V(t-2)
-  static constexpr int kBarDrain = 12;
-  static constexpr int kNumBars = 13;
+  static constexpr int kBarPVD = 3;               // [3] PV(g) complete
+  static constexpr int kBarKVF = 6;               // [3] stage t: K(t) (+Q), V(t-2) landed; P(t-2) written
+  static constexpr int kBarDrain = 9;
+  static constexpr int kNumBars = 10;
   static constexpr int kBarBytes = 128;           // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
@@ -188,8 +186,9 @@ struct StepCursor {
 
 // ----------------------------------------------------------------- producer
 
+// Returns the number of stages armed.
 template <int BLK, int D>
-__device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorMap* tm_q,
+__device__ __forceinline__ int fwd_producer(const FwdParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
@@ -262,6 +261,8 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
     }
     const uint32_t fb = bar(C::kBarKVF + t % 3);
     const uint32_t bytes = (first ? C::kQTile : 0) + (r0.nblk + rv.nblk) * BLK * D * 2;
+    // Stages 0 and 1 have no P(t-2): arrive for the softmax warps too.
+    if (t < 2) mbar_arrive_cnt(fb, 4 * C::kNumWG);
     if (bytes > 0) {
       mbar_arrive_expect_tx(fb, bytes);
     } else {
@@ -291,9 +292,21 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
     h1 = r0;
   }
 
-  // Wait until every copy this thread issued has landed (immediate on the normal path).
-  for (int j = (armed > 3 ? armed - 3 : 0); j < armed; ++j)
-    mbar_drain_wait(bar(C::kBarKVF + j % 3), (j / 3) & 1);
+  return armed;
+}
+
+// After an abort: wait for the copies of the last stages the producer armed, which the
+// MMA warp may never have taken.  Their barriers may also lack the softmax warps'
+// arrivals, so those are added first (every role has left its loop by now; on a stage
+// that completed already the extra arrivals fall into an unused phase).
+template <int BLK, int D>
+__device__ __forceinline__ void drain_stages(uint32_t sbase, int armed) {
+  using C = FwdCfg<BLK, D>;
+  for (int j = (armed > 3 ? armed - 3 : 0); j < armed; ++j) {
+    const uint32_t b = sbase + C::kOffBar + 8 * (C::kBarKVF + j % 3);
+    mbar_arrive_cnt(b, 4 * C::kNumWG);
+    mbar_drain_wait(b, (j / 3) & 1);
+  }
 }
 
 // --------------------------------------------------------------- MMA issuer
@@ -354,11 +367,9 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
                      kk > 0 ? 1u : 0u);
       tc_commit(bar(C::kBarSF + t % 3));
     };
-    // P(t-2) written by the softmax (and, on an item's first step, O read out).
-    auto issue_pv = [&]() -> bool {
-      if (!mbar_wait(bar(C::kBarPF + (t - 2) % 3), ((t - 2) / 3) & 1, ctl, kSiteMmaPFull))
-        return false;
-      tc_fence_after();
+    // P(t-2) is written (and, on an item's first step, O read out): stage t's barrier
+    // covered it.
+    auto issue_pv = [&]() {
       const uint32_t ps = tmem + ((t - 2) % 3) * 128;
       const uint32_t od = tmem + C::kOCol;
       const uint32_t vlo = v_lo0 + ((t - 2) % C::kNV) * kTileStep;
@@ -369,12 +380,11 @@ __device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint
         if (kk < ksteps)
           tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
       tc_commit(bar(C::kBarPVD + (t - 2) % 3));
-      return true;
     };
     // S(t) first, so the scores keep their lead.  (Issuing an item's last PV first shortens
     // the softmax's wait at the item boundary, but measured slower on long rows.)
     if (r0.nblk > 0) issue_s();
-    if (pv.nblk > 0 && !issue_pv()) break;
+    if (pv.nblk > 0) issue_pv();
     h2 = h1;
     h1 = r0;
     // Stage t+1, checked while the MMAs just issued are still queued.
@@ -609,7 +619,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
         read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
       }
       tmem_st_wait();
-      warp_arrive(C::kBarPF + g % 3);
+      warp_arrive(C::kBarKVF + (g + 2) % 3);
       if (s == 0 && have_pending) {
         store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
         have_pending = false;
@@ -649,9 +659,8 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
     for (int x = 0; x < 3; ++x) {
       mbar_init(bar(C::kBarSF + x), 1);
-      mbar_init(bar(C::kBarPF + x), 4 * C::kNumWG);
       mbar_init(bar(C::kBarPVD + x), 1);
-      mbar_init(bar(C::kBarKVF + x), 1);
+      mbar_init(bar(C::kBarKVF + x), 1 + 4 * C::kNumWG);
     }
     mbar_init(bar(C::kBarDrain), 1);
     *abort_flag = 0;
@@ -672,8 +681,9 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
 
+  int armed = 0;
   if (warp == 0) {
-    if (lane == 0) fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
+    if (lane == 0) armed = fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
   } else if (warp == 1) {
     if (lane == 0) fwd_mma<BLK, D>(p, sbase, tmem, ctl);
   } else {
@@ -682,6 +692,9 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // On the normal path every stage was consumed by MMAs that have completed (the MMA
+  // warp's drain), so no copy is in flight.
+  if (warp == 0 && lane == 0 && *abort_flag) drain_stages<BLK, D>(sbase, armed);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

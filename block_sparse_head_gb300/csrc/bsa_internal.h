@@ -47,7 +47,6 @@ struct FwdParams {
 enum WaitSite : int {
   kSiteProdKEmpty = 1,
   kSiteProdVEmpty = 2,
-  kSiteMmaPFull = 7,
   kSiteMmaStage = 6,
   kSiteSoftSFull = 9,
   kSiteSoftPvDone = 11,
