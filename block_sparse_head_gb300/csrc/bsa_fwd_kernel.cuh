@@ -13,16 +13,16 @@
 // A CTA walks its share of the work list as one continuous stream of steps g = 0, 1, ...
 //
 // GB300 mapping.  One CTA per SM, warp-specialised:
-//   warp 0      TMA producer.  Stage t brings K(t) (plus the Q tile when step t opens an
-//               item) and V(t-2) into shared memory.  Its barrier also takes one arrive
-//               per softmax warp for P(t-2), so the MMA warp waits once per step, for
-//               its operands and the softmax's P together.
-//   warp 1      tcgen05 issuer (one thread) and TMEM owner.  TMEM holds three S buffers
-//               and one O accumulator.  Iteration t issues S(t) = Q K(t)^T into S[t % 3]
-//               (which P(t-3) occupied; its PV went out in the previous iteration), then
-//               O += P(t-2) V(t-2): sixteen MMAs back to back, then one barrier check for
-//               the next iteration.  The tensor pipe takes only a couple of MMAs ahead of
-//               issue, so every check or stall of the issuing thread idles the pipe.
+//   warp 0      TMA producer.  For step t it loads K(t) (plus the Q tile when t opens an
+//               item) on one barrier and V(t-2) on another.
+//   warp 1      S issuer (one thread) and TMEM owner.  TMEM holds three S buffers and one
+//               O accumulator.  Step t: S(t) = Q K(t)^T into S[t % 3] once K(t) landed
+//               and PV(t-3), the last reader of that buffer, completed.
+//   last warp   PV issuer (one thread).  Step g: O += P(g) V(g), reading P from S[g % 3],
+//               once the softmax wrote P(g) and V(g) landed.
+//               Two issuing threads keep the tensor pipe fed: it takes only a couple of
+//               MMAs ahead of issue, so a lone issuer idles it at every barrier check;
+//               the two streams order themselves through completion barriers only.
 //   softmax     b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
 //               quadrant, lane t and t+16 holding the two 64-key halves of one row.
 //               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
@@ -55,7 +55,8 @@ struct FwdCfg {
   static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // softmax warpgroups
-  static constexpr int kThreads = 64 + 128 * kNumWG;  // producer warp, MMA warp, softmax
+  static constexpr int kPvWarp = 2 + 4 * kNumWG;       // after the softmax warps
+  static constexpr int kThreads = 32 * (kPvWarp + 1);  // producer, S issuer, softmax, PV issuer
   static constexpr int kKR = 128;                 // key rows per step
   static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
   static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
@@ -77,10 +78,13 @@ struct FwdCfg {
   // barrier indices
   static constexpr int kBarSF = 0;                // [3] S(g) computed
   static constexpr int kBarPVD = 3;               // [3] PV(g) complete
-  static constexpr int kBarKVF = 6;               // [3] stage t: K(t) (+Q), V(t-2) landed; P(t-2) written
-  static constexpr int kBarDrain = 9;
-  static constexpr int kNumBars = 10;
-  static constexpr int kBarBytes = 128;           // barriers, TMEM slot, abort flag
+  static constexpr int kBarKF = 6;                // [3] K(t) (+Q) landed
+  static constexpr int kBarVF = 9;                // [3] V(g) landed
+  static constexpr int kBarPF = 12;               // [3] P(g) written, O free (one arrive per softmax warp)
+  static constexpr int kBarDrainS = 15;
+  static constexpr int kBarDrainP = 16;
+  static constexpr int kNumBars = 17;
+  static constexpr int kBarBytes = 192;           // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -186,13 +190,13 @@ struct StepCursor {
 
 // ----------------------------------------------------------------- producer
 
-// Returns the number of stages armed.
 template <int BLK, int D>
-__device__ __forceinline__ int fwd_producer(const FwdParams& p, const CUtensorMap* tm_q,
+__device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
   constexpr int G = C::kG;
+  static_assert(C::kNK == 3 && C::kNV == 3, "slot reuse is tied to the three S buffers");
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   // Global row of each block of a step (nblk = 0: no step).
   struct StepRows {
@@ -202,7 +206,7 @@ __device__ __forceinline__ int fwd_producer(const FwdParams& p, const CUtensorMa
 
   StepCursor<G> c;
   c.init(p);
-  int colv[G];  // column blocks of the cursor's step, loaded one stage ahead
+  int colv[G];  // column blocks of the cursor's step, loaded one step ahead
   auto fetch_cols = [&]() {
     if (!c.valid()) return;
     const int nb = c.nblk();
@@ -215,7 +219,7 @@ __device__ __forceinline__ int fwd_producer(const FwdParams& p, const CUtensorMa
   StepRows h1{}, h2{};  // steps t-1, t-2
   h1.nblk = h2.nblk = 0;
   int nsteps = -1;  // known once the cursor runs out
-  int armed = 0;
+  int nk = 0, nv = 0;  // K and V loads armed
   for (int t = 0;; ++t) {
     StepRows r0{};
     r0.nblk = 0;
@@ -236,167 +240,147 @@ __device__ __forceinline__ int fwd_producer(const FwdParams& p, const CUtensorMa
         for (int cc = 0; cc < D / 64; ++cc) tma_prefetch_l2_2d(tm_q, cc * 64, nrow);
       }
       c.advance(p);
-      fetch_cols();  // the next step's columns, consumed one stage later
+      fetch_cols();  // the next step's columns, consumed one iteration later
     } else {
       if (nsteps < 0) nsteps = t;
       if (nsteps == 0 || t >= nsteps + 2) break;
     }
-    const StepRows rv = h2;
-    // Stage t re-arms the barrier of stage t-3, so the MMA warp must have taken stage t-3;
-    // S(t-3) completing shows that (every stage t < nsteps + 2 follows a step t-3), and
-    // it also frees K slot t % 3 (kNK = 3).  A stage that opens an item needs its Q
-    // buffer back: with one Q buffer the previous item's last S, S(t-1), must be
-    // complete; with two, the last S of the item before that, which is S(t-2) or earlier.
-    // S completes in issue order, so one wait covers all of it.
-    static_assert(C::kNK == 3, "K slot reuse is tied to the three S buffers");
-    {
+    if (r0.nblk > 0) {
+      // K slot t % 3 held K(t-3), read by S(t-3); S(t-3) completing also shows that the S
+      // issuer took that K barrier phase.  A step that opens an item needs its Q buffer
+      // back: with one Q buffer the previous item's last S, S(t-1), must be complete;
+      // with two, the last S of the item before that, S(t-2) or earlier.  S completes in
+      // issue order, so one wait covers all of it.
       int j = (t >= 3) ? t - 3 : -1;
       if (first) j = max(j, t - (C::kNQ == 1 ? 1 : 2));
       if (j >= 0 && !mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
-    }
-    // V slot (t-2) % kNV held V(t-2-kNV): its PV must be complete.
-    if (rv.nblk > 0 && t - 2 >= C::kNV) {
-      const int j = t - 2 - C::kNV;
-      if (!mbar_wait(bar(C::kBarPVD + j % 3), (j / 3) & 1, ctl, kSiteProdVEmpty)) break;
-    }
-    const uint32_t fb = bar(C::kBarKVF + t % 3);
-    const uint32_t bytes = (first ? C::kQTile : 0) + (r0.nblk + rv.nblk) * BLK * D * 2;
-    // Stages 0 and 1 have no P(t-2): arrive for the softmax warps too.
-    if (t < 2) mbar_arrive_cnt(fb, 4 * C::kNumWG);
-    if (bytes > 0) {
-      mbar_arrive_expect_tx(fb, bytes);
-    } else {
-      mbar_arrive(fb);
-    }
-    ++armed;
-    if (first) {
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc)
-        tma_load_2d(sbase + C::kOffQ + qb * C::kQTile + cc * C::kQRegion, tm_q, fb, cc * 64, qrow);
-    }
-    const uint32_t kdst = sbase + C::kOffK + (t % C::kNK) * C::kKVTile;
-    for (int g = 0; g < r0.nblk; ++g) {
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc)
-        tma_load_2d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, cc * 64, r0.krow[g]);
-    }
-    if (rv.nblk > 0) {
-      const uint32_t vdst = sbase + C::kOffV + ((t - 2) % C::kNV) * C::kKVTile;
-      for (int g = 0; g < rv.nblk; ++g) {
+      const uint32_t fb = bar(C::kBarKF + t % 3);
+      mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * BLK * D * 2);
+      ++nk;
+      if (first) {
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
-          tma_load_2d(vdst + cc * C::kKVRegion + g * BLK * 128, tm_v, fb, cc * 64, rv.krow[g]);
+          tma_load_2d(sbase + C::kOffQ + qb * C::kQTile + cc * C::kQRegion, tm_q, fb, cc * 64, qrow);
+      }
+      const uint32_t kdst = sbase + C::kOffK + (t % 3) * C::kKVTile;
+      for (int g = 0; g < r0.nblk; ++g) {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc)
+          tma_load_2d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, cc * 64, r0.krow[g]);
+      }
+    }
+    const StepRows rv = h2;
+    if (rv.nblk > 0) {
+      // V slot g % 3 (g = t-2) held V(g-3), read by PV(g-3), which the PV issuer issued
+      // after taking that V barrier phase.
+      const int g = t - 2;
+      if (g >= 3 && !mbar_wait(bar(C::kBarPVD + (g - 3) % 3), ((g - 3) / 3) & 1, ctl, kSiteProdVEmpty))
+        break;
+      const uint32_t fb = bar(C::kBarVF + g % 3);
+      mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
+      ++nv;
+      const uint32_t vdst = sbase + C::kOffV + (g % 3) * C::kKVTile;
+      for (int b = 0; b < rv.nblk; ++b) {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc)
+          tma_load_2d(vdst + cc * C::kKVRegion + b * BLK * 128, tm_v, fb, cc * 64, rv.krow[b]);
       }
     }
     h2 = h1;
     h1 = r0;
   }
 
-  return armed;
+  // Wait until every copy this thread issued has landed (immediate on the normal path).
+  for (int j = (nk > 3 ? nk - 3 : 0); j < nk; ++j)
+    mbar_drain_wait(bar(C::kBarKF + j % 3), (j / 3) & 1);
+  for (int j = (nv > 3 ? nv - 3 : 0); j < nv; ++j)
+    mbar_drain_wait(bar(C::kBarVF + j % 3), (j / 3) & 1);
 }
 
-// After an abort: wait for the copies of the last stages the producer armed, which the
-// MMA warp may never have taken.  Their barriers may also lack the softmax warps'
-// arrivals, so those are added first (every role has left its loop by now; on a stage
-// that completed already the extra arrivals fall into an unused phase).
+// --------------------------------------------------------------- MMA issuers
+
+// Shared-memory descriptors are built once; per MMA only the low word (start address >> 4)
+// moves.  K and Q are K-major, V is MN-major; all three share the high word.
 template <int BLK, int D>
-__device__ __forceinline__ void drain_stages(uint32_t sbase, int armed) {
+struct MmaDescs {
   using C = FwdCfg<BLK, D>;
-  for (int j = (armed > 3 ? armed - 3 : 0); j < armed; ++j) {
-    const uint32_t b = sbase + C::kOffBar + 8 * (C::kBarKVF + j % 3);
-    mbar_arrive_cnt(b, 4 * C::kNumWG);
-    mbar_drain_wait(b, (j / 3) & 1);
+  uint32_t hi, k0, v0, q0;
+  __device__ __forceinline__ explicit MmaDescs(uint32_t sbase) {
+    const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);
+    hi = static_cast<uint32_t>(kdesc0 >> 32);
+    k0 = static_cast<uint32_t>(kdesc0);
+    v0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffV, C::kKVRegion, 1024));
+    q0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffQ, 16, 1024));
   }
-}
+};
 
-// --------------------------------------------------------------- MMA issuer
-
+// S(t) = Q K(t)^T into S[t % 3].
 template <int BLK, int D>
-__device__ __forceinline__ void fwd_mma(const FwdParams& p, uint32_t sbase, uint32_t tmem,
-                                        const WaitCtl& ctl) {
+__device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+                                          const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  // Descriptors are built once; per MMA only the low word (start address >> 4) moves.
-  const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);              // K-major
-  const uint64_t vdesc0 = sdesc_sw128(sbase + C::kOffV, C::kKVRegion, 1024);      // MN-major
-  const uint32_t desc_hi = static_cast<uint32_t>(kdesc0 >> 32);  // same for Q, K and V
-  const uint32_t k_lo0 = static_cast<uint32_t>(kdesc0);
-  const uint32_t v_lo0 = static_cast<uint32_t>(vdesc0);
-  const uint32_t q_lo0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffQ, 16, 1024));
+  const MmaDescs<BLK, D> md(sbase);
   constexpr uint32_t kTileStep = C::kKVTile >> 4;  // descriptor units per K/V tile
-
-  // What an iteration needs of a step (nblk = 0: no step).
-  struct StepInfo {
-    int nblk;
-    int first;  // first step of its item
-    int qb;     // Q buffer of its item
-  };
   StepCursor<G> c;
   c.init(p);
-  StepInfo h1{0, 0, 0}, h2{0, 0, 0};  // steps t-1, t-2
-  int nsteps = -1;  // known once the cursor runs out
-  bool ok = true;
-  if (c.valid()) {
-    ok = mbar_wait(bar(C::kBarKVF), 0, ctl, kSiteMmaStage);
-  } else {
-    nsteps = 0;
-  }
-  for (int t = 0; ok && nsteps != 0; ++t) {
-    StepInfo r0{0, 0, 0};
-    if (c.valid()) {
-      r0.nblk = c.nblk();
-      r0.first = (c.s == 0);
-      r0.qb = c.is.n % C::kNQ;
-      c.advance(p);
-      if (!c.valid()) nsteps = t + 1;
-    }
-    if (nsteps >= 0 && t >= nsteps + 2) break;
-    const StepInfo pv = h2;
-    // Stage t has landed (checked at the end of the previous iteration).
+  for (int t = 0; c.valid(); ++t) {
+    const int nblk = c.nblk();
+    const int qb = c.is.n % C::kNQ;
+    c.advance(p);
+    if (!mbar_wait(bar(C::kBarKF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
+    // S[t % 3] was last read by PV(t-3).
+    if (t >= 3 && !mbar_wait(bar(C::kBarPVD + t % 3), ((t - 3) / 3) & 1, ctl, kSiteMmaPvDone)) break;
     tc_fence_after();
-    auto issue_s = [&]() {
-      const uint32_t sbuf = tmem + (t % 3) * 128;
-      const uint32_t qlo = q_lo0 + r0.qb * (C::kQTile >> 4);
-      const uint32_t klo = k_lo0 + (t % C::kNK) * kTileStep;
-      const uint32_t idesc = (r0.nblk == G) ? C::kIdescS : C::kIdescS1;
+    const uint32_t sb = tmem + (t % 3) * 128;
+    const uint32_t qlo = md.q0 + qb * (C::kQTile >> 4);
+    const uint32_t klo = md.k0 + (t % 3) * kTileStep;
+    const uint32_t idesc = (nblk == G) ? C::kIdescS : C::kIdescS1;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_ss_lh(sbuf, qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), desc_hi,
-                     klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), desc_hi, idesc,
-                     kk > 0 ? 1u : 0u);
-      tc_commit(bar(C::kBarSF + t % 3));
-    };
-    // P(t-2) is written (and, on an item's first step, O read out): stage t's barrier
-    // covered it.
-    auto issue_pv = [&]() {
-      const uint32_t ps = tmem + ((t - 2) % 3) * 128;
-      const uint32_t od = tmem + C::kOCol;
-      const uint32_t vlo = v_lo0 + ((t - 2) % C::kNV) * kTileStep;
-      const int ksteps = pv.nblk * BLK / 16;
-      tc_mma_ts_lh(od, ps, vlo, desc_hi, C::kIdescPV, pv.first ? 0u : 1u);
-#pragma unroll
-      for (int kk = 1; kk < C::kKR / 16; ++kk)
-        if (kk < ksteps)
-          tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), desc_hi, C::kIdescPV, 1u);
-      tc_commit(bar(C::kBarPVD + (t - 2) % 3));
-    };
-    // S(t) first, so the scores keep their lead.  (Issuing an item's last PV first shortens
-    // the softmax's wait at the item boundary, but measured slower on long rows.)
-    if (r0.nblk > 0) issue_s();
-    if (pv.nblk > 0) issue_pv();
-    h2 = h1;
-    h1 = r0;
-    // Stage t+1, checked while the MMAs just issued are still queued.
-    const int tn = t + 1;
-    if ((nsteps < 0 || tn < nsteps + 2) &&
-        !mbar_wait(bar(C::kBarKVF + tn % 3), (tn / 3) & 1, ctl, kSiteMmaStage))
-      break;
+    for (int kk = 0; kk < D / 16; ++kk)
+      tc_mma_ss_lh(sb, qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), md.hi,
+                   klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), md.hi, idesc,
+                   kk > 0 ? 1u : 0u);
+    tc_commit(bar(C::kBarSF + t % 3));
   }
+  // Let every MMA this thread issued finish before TMEM is released.
+  tc_commit(bar(C::kBarDrainS));
+  mbar_drain_wait(bar(C::kBarDrainS), 0);
+}
 
-  // Let every MMA issued so far finish before TMEM is released.
-  tc_commit(bar(C::kBarDrain));
-  mbar_drain_wait(bar(C::kBarDrain), 0);
+// O += P(g) V(g), P read from S[g % 3].
+template <int BLK, int D>
+__device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+                                           const WaitCtl& ctl) {
+  using C = FwdCfg<BLK, D>;
+  constexpr int G = C::kG;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const MmaDescs<BLK, D> md(sbase);
+  constexpr uint32_t kTileStep = C::kKVTile >> 4;
+  StepCursor<G> c;
+  c.init(p);
+  for (int g = 0; c.valid(); ++g) {
+    const int nblk = c.nblk();
+    const bool first = (c.s == 0);
+    c.advance(p);
+    // P(g) written (and, on an item's first step, O read out), V(g) landed.
+    if (!mbar_wait(bar(C::kBarPF + g % 3), (g / 3) & 1, ctl, kSiteMmaPFull)) break;
+    if (!mbar_wait(bar(C::kBarVF + g % 3), (g / 3) & 1, ctl, kSiteMmaStage)) break;
+    tc_fence_after();
+    const uint32_t ps = tmem + (g % 3) * 128;
+    const uint32_t od = tmem + C::kOCol;
+    const uint32_t vlo = md.v0 + (g % 3) * kTileStep;
+    const int ksteps = nblk * BLK / 16;
+    tc_mma_ts_lh(od, ps, vlo, md.hi, C::kIdescPV, first ? 0u : 1u);
+#pragma unroll
+    for (int kk = 1; kk < C::kKR / 16; ++kk)
+      if (kk < ksteps)
+        tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), md.hi, C::kIdescPV, 1u);
+    tc_commit(bar(C::kBarPVD + g % 3));
+  }
+  tc_commit(bar(C::kBarDrainP));
+  mbar_drain_wait(bar(C::kBarDrainP), 0);
 }
 
 // ------------------------------------------------------------ softmax group
@@ -619,7 +603,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
         read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
       }
       tmem_st_wait();
-      warp_arrive(C::kBarKVF + (g + 2) % 3);
+      warp_arrive(C::kBarPF + g % 3);
       if (s == 0 && have_pending) {
         store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
         have_pending = false;
@@ -660,9 +644,12 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
     for (int x = 0; x < 3; ++x) {
       mbar_init(bar(C::kBarSF + x), 1);
       mbar_init(bar(C::kBarPVD + x), 1);
-      mbar_init(bar(C::kBarKVF + x), 1 + 4 * C::kNumWG);
+      mbar_init(bar(C::kBarKF + x), 1);
+      mbar_init(bar(C::kBarVF + x), 1);
+      mbar_init(bar(C::kBarPF + x), 4 * C::kNumWG);
     }
-    mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarDrainS), 1);
+    mbar_init(bar(C::kBarDrainP), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -681,20 +668,18 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
 
-  int armed = 0;
   if (warp == 0) {
-    if (lane == 0) armed = fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
+    if (lane == 0) fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
   } else if (warp == 1) {
-    if (lane == 0) fwd_mma<BLK, D>(p, sbase, tmem, ctl);
+    if (lane == 0) fwd_mma_s<BLK, D>(p, sbase, tmem, ctl);
+  } else if (warp == C::kPvWarp) {
+    if (lane == 0) fwd_mma_pv<BLK, D>(p, sbase, tmem, ctl);
   } else {
     fwd_softmax<BLK, D>(p, sbase, tmem, ctl);
   }
 
   tc_fence_before();
   __syncthreads();
-  // On the normal path every stage was consumed by MMAs that have completed (the MMA
-  // warp's drain), so no copy is in flight.
-  if (warp == 0 && lane == 0 && *abort_flag) drain_stages<BLK, D>(sbase, armed);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -48,6 +48,8 @@ enum WaitSite : int {
   kSiteProdKEmpty = 1,
   kSiteProdVEmpty = 2,
   kSiteMmaStage = 6,
+  kSiteMmaPFull = 7,
+  kSiteMmaPvDone = 8,
   kSiteSoftSFull = 9,
   kSiteSoftPvDone = 11,
   kSiteSoftItemDone = 12,
