@@ -61,11 +61,15 @@ struct FwdCfg {
   static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
   static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
   static constexpr int kNK = 3;                   // K tiles in shared memory
-  static constexpr int kNV = 3;                   // V tiles in shared memory
+  static constexpr int kQTileB = BLK * D * 2;     // (bytes of one Q tile, for the budget below)
+  static constexpr int kKVTileB = 128 * D * 2;
+  // Two Q tiles, so the next item's Q loads while the current item's last S runs; V gets
+  // three tiles when they fit beside them, else two (b = 128, d = 128).
+  static constexpr int kNV = (2 * kQTileB + 6 * kKVTileB + 1216 <= 232448) ? 3 : 2;  // V tiles
   static constexpr int kQTile = BLK * D * 2;      // bytes of one Q tile
   static constexpr int kKVTile = kKR * D * 2;     // bytes of one K or V step tile
   // Q tiles: two when they fit beside the K/V tiles, else one (b = 128, d = 128).
-  static constexpr int kNQ = (2 * kQTile + (kNK + kNV) * kKVTile + 1152 <= 232448) ? 2 : 1;
+  static constexpr int kNQ = 2;
   static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
   static constexpr int kKVRegion = kKR * 128;     // one 64-column box of a step tile
   static constexpr int kOCol = kNS * 128;         // O after the S buffers
@@ -196,7 +200,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = FwdCfg<BLK, D>;
   constexpr int G = C::kG;
-  static_assert(C::kNK == 3 && C::kNV == 3, "slot reuse is tied to the three S buffers");
+  static_assert(C::kNK == 3, "K slot reuse is tied to the three S buffers");
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   // Global row of each block of a step (nblk = 0: no step).
   struct StepRows {
@@ -271,15 +275,16 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
     }
     const StepRows rv = h2;
     if (rv.nblk > 0) {
-      // V slot g % 3 (g = t-2) held V(g-3), read by PV(g-3), which the PV issuer issued
-      // after taking that V barrier phase.
+      // V slot g % kNV (g = t-2) held V(g-kNV), read by PV(g-kNV), which the PV issuer
+      // issued after taking that V barrier phase.
       const int g = t - 2;
-      if (g >= 3 && !mbar_wait(bar(C::kBarPVD + (g - 3) % 3), ((g - 3) / 3) & 1, ctl, kSiteProdVEmpty))
+      const int gv = g - C::kNV;
+      if (gv >= 0 && !mbar_wait(bar(C::kBarPVD + gv % 3), (gv / 3) & 1, ctl, kSiteProdVEmpty))
         break;
       const uint32_t fb = bar(C::kBarVF + g % 3);
       mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
       ++nv;
-      const uint32_t vdst = sbase + C::kOffV + (g % 3) * C::kKVTile;
+      const uint32_t vdst = sbase + C::kOffV + (g % C::kNV) * C::kKVTile;
       for (int b = 0; b < rv.nblk; ++b) {
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
@@ -370,7 +375,7 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
     tc_fence_after();
     const uint32_t ps = tmem + (g % 3) * 128;
     const uint32_t od = tmem + C::kOCol;
-    const uint32_t vlo = md.v0 + (g % 3) * kTileStep;
+    const uint32_t vlo = md.v0 + (g % C::kNV) * kTileStep;
     const int ksteps = nblk * BLK / 16;
     tc_mma_ts_lh(od, ps, vlo, md.hi, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
