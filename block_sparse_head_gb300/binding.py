@@ -25,7 +25,8 @@ BSA_ERR_DEVICE_TIMEOUT = -8
 
 # Every symbol declared in include/bsa.h.
 EXPORTED = (
-    "bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_upload", "bsa_lut_free",
+    "bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule", "bsa_lut_upload",
+    "bsa_lut_free",
     "bsa_forward", "bsa_device_status", "bsa_set_wait_limit", "bsa_wait_selftest",
     "bsa_status_string", "bsa_version", "bsa_forward_noalloc",
 )
@@ -64,6 +65,7 @@ def load_library():
                                       ctypes.POINTER(vp)]
         lib.bsa_lut_info.argtypes = [vp, ip, ip, ip, ip, ip]
         lib.bsa_lut_export.argtypes = [vp, vp, vp, vp]
+        lib.bsa_lut_schedule.argtypes = [vp, ctypes.c_int, vp, vp]
         lib.bsa_lut_upload.argtypes = [vp, vp]
         lib.bsa_lut_free.argtypes = [vp]
         lib.bsa_lut_free.restype = None
@@ -81,7 +83,8 @@ def load_library():
         lib.bsa_status_string.restype = ctypes.c_char_p
         lib.bsa_version.argtypes = []
         lib.bsa_version.restype = ctypes.c_char_p
-        for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_upload",
+        for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule",
+                     "bsa_lut_upload",
                      "bsa_forward", "bsa_device_status", "bsa_set_wait_limit",
                      "bsa_wait_selftest"):
             getattr(lib, name).restype = ctypes.c_int
@@ -128,6 +131,15 @@ class Lut:
         _check(self._lib.bsa_lut_export(self.handle, rp.ctypes.data, ci.ctypes.data, it.ctypes.data),
                "bsa_lut_export")
         return rp, ci[:self.nnz_total], it
+
+    def schedule(self, grid: int):
+        """(items [n_items, 4], cta_start [grid + 1]) of the per-CTA schedule for ``grid``
+        CTAs: CTA c runs items[cta_start[c]:cta_start[c + 1]]."""
+        it = np.empty((max(self.n_items, 1), 4), np.int32)
+        cs = np.empty(int(grid) + 1, np.int32)
+        _check(self._lib.bsa_lut_schedule(self.handle, int(grid), it.ctypes.data, cs.ctypes.data),
+               "bsa_lut_schedule")
+        return it[:self.n_items], cs
 
     def upload(self, stream=None):
         _check(self._lib.bsa_lut_upload(self.handle, _stream_handle(stream)), "bsa_lut_upload")

@@ -118,11 +118,12 @@ __device__ __forceinline__ int step_blocks(int nnz, int s) {
   return rem < G ? rem : G;
 }
 
-// The CTA's share of the work list (items blockIdx.x + k*gridDim.x, k = 0, 1, ...).
+// The CTA's share of the work list: items[cta_start[c] .. cta_start[c+1]) for CTA c.
 // Records are fetched two items ahead and each item's CSR row start and diagonal
 // position one item ahead of use.  A record with w = -1 marks the end.
 struct ItemStream {
-  int k;                 // position of the current item in the CTA's share
+  int t;                 // work-list index of the current item
+  int end;               // one past the CTA's last item
   int n;                 // index of the current item among the non-empty ones
   int4 cur;              // {b, h, i, nnz}
   int cur_rs, cur_dp;    // first CSR entry of its row, position of block i in it (-1: none)
@@ -130,9 +131,8 @@ struct ItemStream {
   int nx1_rs, nx1_dp;
   int4 nx2;
 
-  __device__ __forceinline__ static int4 fetch(const FwdParams& p, int k) {
-    const int t = blockIdx.x + k * gridDim.x;
-    return t < p.n_items ? p.items[t] : make_int4(0, 0, 0, -1);
+  __device__ __forceinline__ int4 fetch(const FwdParams& p, int u) const {
+    return u < end ? p.items[u] : make_int4(0, 0, 0, -1);
   }
   __device__ __forceinline__ static void fetch_aux(const FwdParams& p, const int4& r, int& rs,
                                                    int& dp) {
@@ -148,24 +148,25 @@ struct ItemStream {
   template <bool kSkipEmpty>
   __device__ __forceinline__ void next(const FwdParams& p) {
     for (;;) {
-      ++k;
+      ++t;
       cur = nx1;
       cur_rs = nx1_rs;
       cur_dp = nx1_dp;
       nx1 = nx2;
       fetch_aux(p, nx1, nx1_rs, nx1_dp);
-      nx2 = fetch(p, k + 2);
+      nx2 = fetch(p, t + 2);
       if (cur.w > 0) ++n;
       if (!kSkipEmpty || cur.w != 0) return;
     }
   }
   template <bool kSkipEmpty>
   __device__ __forceinline__ void init(const FwdParams& p) {
-    k = -1;
+    t = p.cta_start[blockIdx.x] - 1;
+    end = p.cta_start[blockIdx.x + 1];
     n = -1;
-    nx1 = fetch(p, 0);
+    nx1 = fetch(p, t + 1);
     fetch_aux(p, nx1, nx1_rs, nx1_dp);
-    nx2 = fetch(p, 1);
+    nx2 = fetch(p, t + 2);
     next<kSkipEmpty>(p);
   }
   __device__ __forceinline__ bool done() const { return cur.w < 0; }

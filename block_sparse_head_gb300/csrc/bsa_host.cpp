@@ -71,13 +71,58 @@ int sm_count(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+// Longest-processing-time-first assignment of the work list to `grid` CTAs.  Items are
+// taken in work-list order (descending block count) and each goes to the CTA with the
+// least work so far (ties: lowest index); an item costs 4 per active block plus 2 for
+// its fixed per-item work (Q load, output write), so empty items spread out too.  Each
+// CTA then walks its own items in the order it received them.  Round-robin assignment
+// of the same list left the busiest CTA 4 % above the mean on the window workload.
+void bsa::build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& items,
+                         std::vector<int32_t>& start) {
+  const int n = lut.n_items;
+  std::vector<int32_t> owner(static_cast<size_t>(n));
+  std::vector<int32_t> count(static_cast<size_t>(grid), 0);
+  // min-heap of (load, cta)
+  using Load = std::pair<int64_t, int32_t>;
+  std::vector<Load> heap;
+  heap.reserve(static_cast<size_t>(grid));
+  for (int c = 0; c < grid; ++c) heap.emplace_back(0, c);
+  auto cmp = [](const Load& a, const Load& b) {
+    return a.first != b.first ? a.first > b.first : a.second > b.second;
+  };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  for (int k = 0; k < n; ++k) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    Load& top = heap.back();
+    owner[static_cast<size_t>(k)] = top.second;
+    ++count[static_cast<size_t>(top.second)];
+    top.first += 4 * static_cast<int64_t>(lut.items[static_cast<size_t>(k) * 4 + 3]) + 2;
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  start.assign(static_cast<size_t>(grid) + 1, 0);
+  for (int c = 0; c < grid; ++c)
+    start[static_cast<size_t>(c) + 1] = start[static_cast<size_t>(c)] + count[static_cast<size_t>(c)];
+  std::vector<int32_t> fill(start.begin(), start.end() - 1);
+  items.assign(static_cast<size_t>(n) * 4, 0);
+  for (int k = 0; k < n; ++k) {
+    const int32_t pos = fill[static_cast<size_t>(owner[static_cast<size_t>(k)])]++;
+    std::memcpy(&items[static_cast<size_t>(pos) * 4], &lut.items[static_cast<size_t>(k) * 4], 16);
+  }
+}
+
+namespace {
+
 void free_device(bsa_lut* lut) {
   if (lut->d_row_ptr) cudaFree(lut->d_row_ptr);
   if (lut->d_col_idx) cudaFree(lut->d_col_idx);
   if (lut->d_items) cudaFree(lut->d_items);
   if (lut->d_status) cudaFree(lut->d_status);
   if (lut->d_diag_pos) cudaFree(lut->d_diag_pos);
+  if (lut->d_sched_start) cudaFree(lut->d_sched_start);
   lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = lut->d_diag_pos = nullptr;
+  lut->d_sched_start = nullptr;
   lut->device = -1;
 }
 
@@ -172,18 +217,43 @@ int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32
   return BSA_OK;
 }
 
+int bsa_lut_schedule(const bsa_lut* lut, int grid, int32_t* items, int32_t* cta_start) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (grid < 1 || grid > std::max(1, lut->n_items)) return BSA_ERR_SHAPE;
+  std::vector<int32_t> it, st;
+  try {
+    bsa::build_schedule(*lut, grid, it, st);
+  } catch (const std::bad_alloc&) {
+    return BSA_ERR_ALLOC;
+  }
+  if (items && !it.empty()) std::memcpy(items, it.data(), it.size() * 4);
+  if (cta_start) std::memcpy(cta_start, st.data(), st.size() * 4);
+  return BSA_OK;
+}
+
 int bsa_lut_upload(bsa_lut* lut, void* stream) {
   if (lut == nullptr) return BSA_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
   free_device(lut);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return BSA_ERR_CUDA;
+  lut->sched_grid = std::max(1, std::min(lut->n_items, sms));
+  try {
+    bsa::build_schedule(*lut, lut->sched_grid, lut->sched_items, lut->sched_start);
+  } catch (const std::bad_alloc&) {
+    lut->sched_grid = 0;
+    return BSA_ERR_ALLOC;
+  }
   const size_t nr = lut->row_ptr.size() * 4;
   const size_t nc = std::max<size_t>(lut->col_idx.size(), 1) * 4;
-  const size_t ni = lut->items.size() * 4;
+  const size_t ni = std::max<size_t>(lut->items.size(), 4) * 4;
+  const size_t ns = lut->sched_start.size() * 4;
   if (cudaMalloc(&lut->d_row_ptr, nr) != cudaSuccess || cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess ||
       cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess ||
-      cudaMalloc(&lut->d_diag_pos, lut->diag_pos.size() * 4) != cudaSuccess) {
+      cudaMalloc(&lut->d_diag_pos, lut->diag_pos.size() * 4) != cudaSuccess ||
+      cudaMalloc(&lut->d_sched_start, ns) != cudaSuccess) {
     free_device(lut);
     cudaGetLastError();
     return BSA_ERR_ALLOC;
@@ -193,8 +263,11 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
             (lut->col_idx.empty() ||
              cudaMemcpyAsync(lut->d_col_idx, lut->col_idx.data(), lut->col_idx.size() * 4,
                              cudaMemcpyHostToDevice, st) == cudaSuccess) &&
-            cudaMemcpyAsync(lut->d_items, lut->items.data(), ni, cudaMemcpyHostToDevice, st) ==
-                cudaSuccess &&
+            (lut->sched_items.empty() ||
+             cudaMemcpyAsync(lut->d_items, lut->sched_items.data(), lut->sched_items.size() * 4,
+                             cudaMemcpyHostToDevice, st) == cudaSuccess) &&
+            cudaMemcpyAsync(lut->d_sched_start, lut->sched_start.data(), ns, cudaMemcpyHostToDevice,
+                            st) == cudaSuccess &&
             cudaMemcpyAsync(lut->d_diag_pos, lut->diag_pos.data(), lut->diag_pos.size() * 4,
                             cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
@@ -239,6 +312,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
 
   bsa::FwdParams p{};
   p.items = reinterpret_cast<const int4*>(lut->d_items);
+  p.cta_start = lut->d_sched_start;
   p.row_ptr = lut->d_row_ptr;
   p.col_idx = lut->d_col_idx;
   p.diag_pos = lut->d_diag_pos;
@@ -253,9 +327,8 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
 
-  const int sms = sm_count(dev);
-  if (sms <= 0) return BSA_ERR_CUDA;
-  const int grid = std::max(1, std::min(lut->n_items, sms));
+  const int grid = lut->sched_grid;  // the schedule uploaded with the LUT
+  if (grid <= 0) return BSA_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (block == 128 && d == 128)

@@ -15,6 +15,11 @@ struct bsa_lut {
   std::vector<int32_t> col_idx;  // [nnz_total]
   std::vector<int32_t> items;    // [n_items][4] = {b, h, i, nnz}
   std::vector<int32_t> diag_pos; // [H*nb]: index of block i in row (h, i), or -1
+  // Device schedule for `sched_grid` CTAs (built at upload): the work list regrouped
+  // so that CTA c takes sched_items[sched_start[c] .. sched_start[c+1]).
+  int sched_grid = 0;
+  std::vector<int32_t> sched_items;  // [n_items][4]
+  std::vector<int32_t> sched_start;  // [sched_grid + 1]
   // device copies (valid after bsa_lut_upload)
   int device = -1;
   int32_t* d_row_ptr = nullptr;
@@ -22,6 +27,7 @@ struct bsa_lut {
   int32_t* d_items = nullptr;
   int32_t* d_diag_pos = nullptr;
   int32_t* d_status = nullptr;
+  int32_t* d_sched_start = nullptr;  // device copy of sched_start (d_items holds sched_items)
   uint64_t wait_limit_ns = 10000000000ull;
 };
 
@@ -29,7 +35,8 @@ namespace bsa {
 
 // Kernel arguments besides the three tensor maps.
 struct FwdParams {
-  const int4* items;        // work list {b, h, i, nnz}
+  const int4* items;        // work list {b, h, i, nnz}, regrouped per CTA
+  const int32_t* cta_start; // CTA c takes items[cta_start[c] .. cta_start[c+1])
   const int32_t* row_ptr;   // CSR row starts over rows h*nb + i
   const int32_t* col_idx;   // active column blocks, ascending per row
   const int32_t* diag_pos;  // per row h*nb + i: position of block i in the row, or -1
@@ -55,6 +62,10 @@ enum WaitSite : int {
   kSiteSoftItemDone = 12,
   kSiteSelftest = 15,
 };
+
+// Regroups lut's work list for `grid` CTAs: CTA c takes items[start[c] .. start[c+1]).
+void build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& items,
+                    std::vector<int32_t>& start);
 
 // One launcher per supported (block, head_dim) pair; each lives in its own
 // translation unit so the variants compile in parallel.

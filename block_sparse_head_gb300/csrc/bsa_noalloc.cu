@@ -16,8 +16,11 @@
 // host threads racing) corrupt each other's LUT.  Serialize them on one stream.
 #include "../../include/bsa.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <new>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -27,11 +30,14 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = 4u << 20;
 constexpr size_t kNoAllocScratchWords = kNoAllocScratchBytes / 4;
+// Room reserved for the per-CTA starts: grids up to this many CTAs.
+constexpr int kMaxGrid = 1023;
 
 // Layout, in int32 words, each part starting on a 16-byte boundary:
 //   [0, 4)           status word (+ padding)
-//   [4, 4 + 4n)      work list, n items of {b, h, i, nnz}
-//   then row_ptr (H*nb + 1 words), then diag_pos (H*nb words), then col_idx (nnz words)
+//   [4, 4 + 4n)      work list, n items of {b, h, i, nnz}, regrouped per CTA
+//   then the per-CTA starts (grid + 1 words), row_ptr (H*nb + 1 words), diag_pos (H*nb
+//   words), col_idx (nnz words)
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 // Device address of g_noalloc_scratch per device, looked up once with that device
@@ -78,7 +84,8 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out) || !a16(lse)) return BSA_ERR_ALIGN;
 
   const size_t off_items = 4;
-  const size_t off_rowptr = off_items + round4(static_cast<size_t>(lut->n_items) * 4);
+  const size_t off_start = off_items + round4(static_cast<size_t>(lut->n_items) * 4);
+  const size_t off_rowptr = off_start + round4(static_cast<size_t>(kMaxGrid) + 1);
   const size_t off_diag = off_rowptr + round4(lut->row_ptr.size());
   const size_t off_colidx = off_diag + round4(lut->diag_pos.size());
   const size_t total = off_colidx + round4(lut->col_idx.size());
@@ -96,6 +103,21 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return BSA_ERR_CUDA;
+  const int grid = std::max(1, std::min({lut->n_items, sms, kMaxGrid}));
+  // The schedule made at upload serves when it was made for this grid; otherwise it is
+  // built here (host memory only).
+  std::vector<int32_t> own_items, own_start;
+  const std::vector<int32_t>* sched_items = &lut->sched_items;
+  const std::vector<int32_t>* sched_start = &lut->sched_start;
+  if (lut->sched_grid != grid || lut->sched_start.empty()) {
+    try {
+      bsa::build_schedule(*lut, grid, own_items, own_start);
+    } catch (const std::bad_alloc&) {
+      return BSA_ERR_ALLOC;
+    }
+    sched_items = &own_items;
+    sched_start = &own_start;
+  }
 
   CUtensorMap tq, tk, tv;
   if (!encode_rows_noalloc(&tq, q, rows, d, block) || !encode_rows_noalloc(&tk, k, rows, d, block) ||
@@ -105,7 +127,10 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status word must start at zero; the LUT parts are overwritten in full.
   if (cudaMemsetAsync(base, 0, 16, st) != cudaSuccess ||
-      cudaMemcpyAsync(base + off_items, lut->items.data(), lut->items.size() * 4,
+      (!sched_items->empty() &&
+       cudaMemcpyAsync(base + off_items, sched_items->data(), sched_items->size() * 4,
+                       cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      cudaMemcpyAsync(base + off_start, sched_start->data(), sched_start->size() * 4,
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(base + off_rowptr, lut->row_ptr.data(), lut->row_ptr.size() * 4,
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -118,6 +143,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
 
   bsa::FwdParams p{};
   p.items = reinterpret_cast<const int4*>(base + off_items);
+  p.cta_start = base + off_start;
   p.row_ptr = base + off_rowptr;
   p.col_idx = base + off_colidx;
   p.diag_pos = base + off_diag;
@@ -131,7 +157,6 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
-  const int grid = lut->n_items < sms ? (lut->n_items > 0 ? lut->n_items : 1) : sms;
   cudaError_t e;
   if (block == 128 && d == 128)
     e = bsa::launch_fwd_b128_d128(p, tq, tk, tv, grid, st);

@@ -102,9 +102,23 @@ int bsa_lut_info(const bsa_lut* lut, int* H, int* nb, int* batch, int* nnz_total
 int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32_t* items);
 
 /*
+ * bsa_lut_schedule -- the per-CTA schedule the kernel runs for a grid of `grid` CTAs
+ * (host only; needs no GPU).  The work list is handed out in its own order, each item
+ * to the CTA with the least work so far (ties: lowest index), an item costing
+ * 4*nnz + 2; CTA c then runs items[4*cta_start[c] .. 4*cta_start[c+1]) in the order it
+ * received them.  items: 4*n_items int32, cta_start: grid+1 int32 (either may be NULL).
+ * bsa_lut_upload uploads this schedule for grid = min(n_items, SM count).
+ * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE (grid < 1 or grid > max(1, n_items)),
+ * BSA_ERR_ALLOC.
+ */
+int bsa_lut_schedule(const bsa_lut* lut, int grid, int32_t* items, int32_t* cta_start);
+
+/*
  * bsa_lut_upload -- allocate device copies of row_ptr, col_idx and the work list
  * (plus a device status word) on the current device and copy them there on
- * `stream`, then synchronize `stream`.  Call once before the first bsa_forward;
+ * `stream`, then synchronize `stream`.  The device work list is the schedule of
+ * bsa_lut_schedule for a grid of min(n_items, SM count of the device); the exported
+ * list keeps its own order.  Call once before the first bsa_forward;
  * calling again re-uploads to the now-current device.  Errors: BSA_ERR_NULL,
  * BSA_ERR_ALLOC, BSA_ERR_CUDA.
  */
@@ -156,9 +170,10 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
  *                call synchronizes `stream` after the kernel and returns
  *                BSA_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel gave up.
  *
- * Limit: 4 + 4*n_items + (H*nb + 1) + H*nb + nnz int32 words (each part rounded up to 4
- * words) must fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before any
- * device work.  The first call on a device looks up the array's device address
+ * Limit: 4 + 4*n_items + 1024 + (H*nb + 1) + H*nb + nnz int32 words (each part rounded
+ * up to 4 words) must fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before
+ * any device work.  The per-CTA schedule comes from bsa_lut_upload when the LUT was
+ * uploaded on this device; otherwise the call builds it in host memory.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any
  * stream capture.  All calls share the array and each call overwrites it: calls
  * whose kernels overlap on the GPU (other streams, other host threads) race, so

@@ -127,3 +127,50 @@ def test_forward_validation_before_device_work(lib):
     assert lib.bsa_device_status(lut.handle, None, None) == -9
     assert lib.bsa_set_wait_limit(None, 5) == -1
     assert lib.bsa_lut_info(None, None, None, None, None, None) == -1
+
+
+def _check_schedule(lut, grid):
+    _, _, items = lut.export()
+    sched, start = lut.schedule(grid)
+    n = lut.n_items
+    assert start[0] == 0 and start[-1] == n and np.all(np.diff(start) >= 0)
+    # every work-list item exactly once; within a CTA in work-list order
+    key = {tuple(r): k for k, r in enumerate(items.tolist())}
+    pos = np.array([key[tuple(r)] for r in sched.tolist()], dtype=np.int64)
+    assert sorted(pos.tolist()) == list(range(n))
+    owner = np.empty(n, np.int64)
+    for c in range(grid):
+        seg = pos[start[c]:start[c + 1]]
+        assert np.all(np.diff(seg) > 0)
+        owner[seg] = c
+    # each item went to a least-loaded CTA (lowest index on ties), replayed in list order
+    cost = 4 * items[:, 3].astype(np.int64) + 2
+    load = np.zeros(grid, np.int64)
+    for k in range(n):
+        assert owner[k] == int(np.argmin(load)), (k, owner[k], load.min())
+        load[owner[k]] += cost[k]
+    # list scheduling bound: the busiest CTA ends at most one item past the mean
+    if n:
+        assert load.max() <= cost.sum() / grid + cost.max()
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_schedule_workloads(lib, index):
+    wl = wls.WORKLOADS[index]
+    lut = binding.Lut(wls.layout_for(wl), wl.B)
+    for grid in (1, 7, 152, lut.n_items):
+        _check_schedule(lut, min(grid, lut.n_items))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_schedule_random_and_errors(lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    H, nb, B = int(rng.integers(1, 5)), int(rng.integers(1, 20)), int(rng.integers(1, 4))
+    lay = wls.random_layout(H, nb, float(rng.uniform(0.0, 1.0)), seed,
+                            empty_rows=int(rng.integers(0, nb + 1)))
+    lut = binding.Lut(lay, B)
+    for grid in sorted({1, 2, 5, lut.n_items}):
+        _check_schedule(lut, grid)
+    for bad in (0, -1, lut.n_items + 1):
+        with pytest.raises(binding.BsaError):
+            lut.schedule(bad)

@@ -133,26 +133,32 @@ def pin_brute(fwd, seed=11, causal=True):
 
 FWDS = [("forward", oracle.forward), ("forward_dense", oracle.forward_dense)]
 
+# Agreement bound for the reductions to library routines.  Both sides are fp64, but
+# the library side (threaded SDPA / logsumexp / BLAS) has been seen to differ from the
+# oracle by up to 6.4e-10 on rare runs of this host; every slip the pins guard against
+# (a dropped term, a flipped mask, a transposed product) moves results by 1e-3 or more.
+LIB_TOL = 1e-9
+
 
 @pytest.mark.parametrize("name,fwd", FWDS)
 def test_dense_layout_is_sdpa(name, fwd):
-    assert pin_dense(fwd) < 1e-12
+    assert pin_dense(fwd) < LIB_TOL
 
 
 @pytest.mark.parametrize("name,fwd", FWDS)
 def test_causal_layout_is_causal_sdpa(name, fwd):
-    assert pin_causal(fwd) < 1e-12
+    assert pin_causal(fwd) < LIB_TOL
 
 
 @pytest.mark.parametrize("name,fwd", FWDS)
 def test_block_diagonal_is_per_block_sdpa(name, fwd):
-    assert pin_block_diagonal(fwd) < 1e-12
+    assert pin_block_diagonal(fwd) < LIB_TOL
 
 
 @pytest.mark.parametrize("name,fwd", FWDS)
 @pytest.mark.parametrize("causal", [False, True])
 def test_brute_force_tiny(name, fwd, causal):
-    assert pin_brute(fwd, causal=causal) < 1e-12
+    assert pin_brute(fwd, causal=causal) < LIB_TOL
 
 
 def test_skip_equals_dense_mask():
