@@ -242,7 +242,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
         // Warm L2 with the following item's Q.
         const int nrow = (c.is.nx1.x * p.H + c.is.nx1.y) * p.L + c.is.nx1.z * BLK;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) tma_prefetch_l2_2d(tm_q, cc * 64, nrow);
+        tma_prefetch_l2_3d(tm_q, 0, nrow, 0);
       }
       c.advance(p);
       fetch_cols();  // the next step's columns, consumed one iteration later
@@ -262,16 +262,17 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       const uint32_t fb = bar(C::kBarKF + t % 3);
       mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * BLK * D * 2);
       ++nk;
-      if (first) {
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc)
-          tma_load_2d(sbase + C::kOffQ + qb * C::kQTile + cc * C::kQRegion, tm_q, fb, cc * 64, qrow);
-      }
+      // One copy per tile with all column halves (K and V of 64-row blocks: one per half).
+      if (first) tma_load_3d(sbase + C::kOffQ + qb * C::kQTile, tm_q, fb, 0, qrow, 0);
       const uint32_t kdst = sbase + C::kOffK + (t % 3) * C::kKVTile;
-      for (int g = 0; g < r0.nblk; ++g) {
+      if (BLK == 128) {
+        tma_load_3d(kdst, tm_k, fb, 0, r0.krow[0], 0);
+      } else {
+        for (int g = 0; g < r0.nblk; ++g) {
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc)
-          tma_load_2d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, cc * 64, r0.krow[g]);
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_load_3d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, 0, r0.krow[g], cc);
+        }
       }
     }
     const StepRows rv = h2;
@@ -286,10 +287,14 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
       ++nv;
       const uint32_t vdst = sbase + C::kOffV + (g % C::kNV) * C::kKVTile;
-      for (int b = 0; b < rv.nblk; ++b) {
+      if (BLK == 128) {
+        tma_load_3d(vdst, tm_v, fb, 0, rv.krow[0], 0);
+      } else {
+        for (int b = 0; b < rv.nblk; ++b) {
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc)
-          tma_load_2d(vdst + cc * C::kKVRegion + b * BLK * 128, tm_v, fb, cc * 64, rv.krow[b]);
+          for (int cc = 0; cc < D / 64; ++cc)
+            tma_load_3d(vdst + cc * C::kKVRegion + b * BLK * 128, tm_v, fb, 0, rv.krow[b], cc);
+        }
       }
     }
     h2 = h1;

@@ -44,16 +44,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows, d] bf16 view of a [B,H,L,d] tensor; box = 64 columns x `box_rows` rows,
-// 128-byte swizzle (matches the kernel's shared-memory operand layout).
-bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows) {
+// [rows, d] bf16 view of a [B,H,L,d] tensor as three dimensions: 64 columns, rows,
+// d/64 column halves (the halves 128 bytes apart, rows d*2 bytes apart).  The box is 64
+// columns x `box_rows` rows x `box_halves` halves with the 128-byte swizzle: one copy
+// lands the halves one after the other, each a swizzled [box_rows][64] region, which is
+// the kernel's shared-memory operand layout.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows,
+                 int box_halves) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_halves)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -306,8 +310,12 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   if (dev != lut->device) return BSA_ERR_STATE;
 
   CUtensorMap tq, tk, tv;
-  if (!encode_rows(&tq, q, rows, d, block) || !encode_rows(&tk, k, rows, d, block) ||
-      !encode_rows(&tv, v, rows, d, block))
+  // K and V of 64-row blocks go one half at a time: a step tile keeps each half's 128
+  // key rows (two blocks) together.
+  const int kv_halves = (block == 128) ? d / 64 : 1;
+  if (!encode_rows(&tq, q, rows, d, block, d / 64) ||
+      !encode_rows(&tk, k, rows, d, block, kv_halves) ||
+      !encode_rows(&tv, v, rows, d, block, kv_halves))
     return BSA_ERR_CUDA;
 
   bsa::FwdParams p{};

@@ -46,7 +46,8 @@ int32_t* g_scratch_addr[64] = {nullptr};
 
 size_t round4(size_t words) { return (words + 3) & ~static_cast<size_t>(3); }
 
-bool encode_rows_noalloc(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows) {
+bool encode_rows_noalloc(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows,
+                         int box_halves) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
     void* ptr = nullptr;
@@ -57,11 +58,12 @@ bool encode_rows_noalloc(CUtensorMap* map, const void* base, int64_t rows, int d
       return false;
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  // Same three-dimensional view as bsa_forward's maps: 64 columns, rows, d/64 halves.
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_halves)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -120,8 +122,10 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   }
 
   CUtensorMap tq, tk, tv;
-  if (!encode_rows_noalloc(&tq, q, rows, d, block) || !encode_rows_noalloc(&tk, k, rows, d, block) ||
-      !encode_rows_noalloc(&tv, v, rows, d, block))
+  const int kv_halves = (block == 128) ? d / 64 : 1;
+  if (!encode_rows_noalloc(&tq, q, rows, d, block, d / 64) ||
+      !encode_rows_noalloc(&tk, k, rows, d, block, kv_halves) ||
+      !encode_rows_noalloc(&tv, v, rows, d, block, kv_halves))
     return BSA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
