@@ -396,15 +396,14 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ softmax group
 
-// O columns [c, c+32) of this thread's half row: lanes 0-15 hold columns c.., lanes
-// 16-31 columns D/2 + c.. of the same rows.
-template <int D>
+// Group c of this thread's O columns: lanes 0-15 hold columns [64c, 64c + 32), lanes
+// 16-31 columns [64c + 32, 64c + 64) of the same rows.  The two lanes of a row thus hold
+// the two halves of one 128-byte line of the bf16 output, which their stores fill together.
 __device__ __forceinline__ void load_o32(uint32_t to, int c, uint32_t (&r)[32]) {
-  tmem_ld_16x32bx2_x32<D / 2>(to + c, r);
+  tmem_ld_16x32bx2_x32<32>(to + c * 64, r);
 }
-template <int D>
 __device__ __forceinline__ void store_o32(uint32_t to, int c, const uint32_t (&r)[32]) {
-  tmem_st_16x32bx2_x32<D / 2>(to + c, r);
+  tmem_st_16x32bx2_x32<32>(to + c * 64, r);
 }
 
 // Reads this thread's half row of O, scales it by inv and packs it to bf16 pairs.
@@ -413,7 +412,7 @@ __device__ __forceinline__ void read_o(uint32_t to, float inv, uint32_t (&pk)[D 
   constexpr int OC = D / 2;
   uint32_t r[OC / 32][32];
 #pragma unroll
-  for (int c = 0; c < OC / 32; ++c) load_o32<D>(to, c * 32, r[c]);
+  for (int c = 0; c < OC / 32; ++c) load_o32(to, c, r[c]);
 #pragma unroll
   for (int c = 0; c < OC / 32; ++c) tmem_ld_wait(r[c]);
 #pragma unroll
@@ -424,24 +423,24 @@ __device__ __forceinline__ void read_o(uint32_t to, float inv, uint32_t (&pk)[D 
           pack_bf16x2(__uint_as_float(r[c][2 * i]) * inv, __uint_as_float(r[c][2 * i + 1]) * inv);
 }
 
-// Stores a packed half row and, from half 0, the lse.  32-byte stores (whole sectors) when
-// the output base allows it, else 16-byte ones.
+// Stores this thread's packed O columns (the load_o32 groups) and, from half 0, the lse.
+// 32-byte stores (whole sectors) when the output base allows it, else 16-byte ones.
 template <int D>
 __device__ __forceinline__ void store_o(const FwdParams& p, int qrow, int half,
                                         const uint32_t (&pk)[D / 4], float m, float l) {
   constexpr int OC = D / 2;
   constexpr float kLn2 = 0.6931471805599453f;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(qrow) * D + half * OC;
+  __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(qrow) * D + half * 32;
   if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
 #pragma unroll
-    for (int q = 0; q < OC / 16; ++q)
-      st_global_v8(dst + 16 * q, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
-                   pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+    for (int q = 0; q < OC / 16; ++q)  // 16 columns per store; group q / 2
+      st_global_v8(row + (q >> 1) * 64 + (q & 1) * 16, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2],
+                   pk[8 * q + 3], pk[8 * q + 4], pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
   } else {
-    uint4* orow = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int q = 0; q < OC / 8; ++q)
-      orow[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    for (int q = 0; q < OC / 8; ++q)  // 8 columns per store; group q / 4
+      *reinterpret_cast<uint4*>(row + (q >> 2) * 64 + (q & 3) * 8) =
+          make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
   }
   if (half == 0) p.lse[qrow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
@@ -598,11 +597,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 #pragma unroll
         for (int c = 0; c < OC / 32; ++c) {
           uint32_t r[32];
-          load_o32<D>(to, c * 32, r);
+          load_o32(to, c, r);
           tmem_ld_wait(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          store_o32<D>(to, c * 32, r);
+          store_o32(to, c, r);
         }
       }
       // First step of an item: the previous item's O (its last PV is g-1) is read out
