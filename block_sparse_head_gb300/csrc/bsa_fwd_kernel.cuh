@@ -476,6 +476,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   bool have_pending = false;
   int pend_row = 0;
   float pend_m = 0.f, pend_l = 0.f;
+  // S(g+1) already complete, as seen by a probe issued during step g (its latency then
+  // overlaps the end of step g instead of opening step g+1).
+  bool s_next = false;
 
   // Every thread of a warp has finished its TMEM traffic: one arrive per warp.
   auto warp_arrive = [&](int b) {
@@ -512,8 +515,12 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       const bool valid = (BLK == 128) || (half < nblk);
       const bool diag = valid && (((BLK == 128) ? s : s * 2 + half) == dpos);
       const uint32_t ts = tl + (g % 3) * 128;
-      ok = wait_bar(C::kBarSF + g % 3, (g / 3) & 1, kSiteSoftSFull);
-      if (!ok) break;
+      if (__all_sync(0xffffffffu, s_next)) {
+        tc_fence_after();
+      } else {
+        ok = wait_bar(C::kBarSF + g % 3, (g / 3) & 1, kSiteSoftSFull);
+        if (!ok) break;
+      }
       float x[NC];
       {
         uint32_t r0[32], r1[32];
@@ -584,6 +591,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
         }
         tmem_st_16x32bx2_x32<32>(ts, pk);
       }
+      // S(g+4) needs this step's P, so the barrier of S(g+1) cannot be a phase ahead.
+      s_next = mbar_test_wait(bar(C::kBarSF + (g + 1) % 3), ((g + 1) / 3) & 1);
       sr2[0] = f2_add(f2_add(sr2[0], sr2[1]), f2_add(sr2[2], sr2[3]));
       float rs = f2_lo(sr2[0]) + f2_hi(sr2[0]);
       rs += __shfl_xor_sync(0xffffffffu, rs, 16);
