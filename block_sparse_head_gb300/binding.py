@@ -65,7 +65,7 @@ def load_library():
                                       ctypes.POINTER(vp)]
         lib.bsa_lut_info.argtypes = [vp, ip, ip, ip, ip, ip]
         lib.bsa_lut_export.argtypes = [vp, vp, vp, vp]
-        lib.bsa_lut_schedule.argtypes = [vp, ctypes.c_int, vp, vp]
+        lib.bsa_lut_schedule.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
         lib.bsa_lut_upload.argtypes = [vp, vp]
         lib.bsa_lut_free.argtypes = [vp]
         lib.bsa_lut_free.restype = None
@@ -132,13 +132,14 @@ class Lut:
                "bsa_lut_export")
         return rp, ci[:self.nnz_total], it
 
-    def schedule(self, grid: int):
+    def schedule(self, grid: int, by_head: bool = False):
         """(items [n_items, 4], cta_start [grid + 1]) of the per-CTA schedule for ``grid``
-        CTAs: CTA c runs items[cta_start[c]:cta_start[c + 1]]."""
+        CTAs: CTA c runs items[cta_start[c]:cta_start[c + 1]].  ``by_head`` hands the items
+        out (batch, head) by (batch, head) instead of in work-list order."""
         it = np.empty((max(self.n_items, 1), 4), np.int32)
         cs = np.empty(int(grid) + 1, np.int32)
-        _check(self._lib.bsa_lut_schedule(self.handle, int(grid), it.ctypes.data, cs.ctypes.data),
-               "bsa_lut_schedule")
+        _check(self._lib.bsa_lut_schedule(self.handle, int(grid), int(bool(by_head)),
+                                          it.ctypes.data, cs.ctypes.data), "bsa_lut_schedule")
         return it[:self.n_items], cs
 
     def upload(self, stream=None):

@@ -83,9 +83,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // its fixed per-item work (Q load, output write), so empty items spread out too.  Each
 // CTA then walks its own items in the order it received them.  Round-robin assignment
 // of the same list left the busiest CTA 4 % above the mean on the window workload.
-void bsa::build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& items,
+// by_head takes the items (batch, head) by (batch, head) instead, keeping the list order
+// within each pair: the CTAs then work on a few pairs at a time, whose K and V stay in L2.
+void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                          std::vector<int32_t>& start) {
   const int n = lut.n_items;
+  std::vector<int32_t> order(static_cast<size_t>(n));
+  for (int k = 0; k < n; ++k) order[static_cast<size_t>(k)] = k;
+  if (by_head) {
+    const int32_t* it = lut.items.data();
+    std::stable_sort(order.begin(), order.end(), [it](int32_t a, int32_t b) {
+      const int32_t* x = it + 4 * static_cast<size_t>(a);
+      const int32_t* y = it + 4 * static_cast<size_t>(b);
+      return x[0] != y[0] ? x[0] < y[0] : x[1] < y[1];
+    });
+  }
   std::vector<int32_t> owner(static_cast<size_t>(n));
   std::vector<int32_t> count(static_cast<size_t>(grid), 0);
   // min-heap of (load, cta)
@@ -102,7 +114,7 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& ite
     Load& top = heap.back();
     owner[static_cast<size_t>(k)] = top.second;
     ++count[static_cast<size_t>(top.second)];
-    top.first += 4 * static_cast<int64_t>(lut.items[static_cast<size_t>(k) * 4 + 3]) + 2;
+    top.first += 4 * static_cast<int64_t>(lut.items[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4 + 3]) + 2;
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
   start.assign(static_cast<size_t>(grid) + 1, 0);
@@ -112,8 +124,20 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& ite
   items.assign(static_cast<size_t>(n) * 4, 0);
   for (int k = 0; k < n; ++k) {
     const int32_t pos = fill[static_cast<size_t>(owner[static_cast<size_t>(k)])]++;
-    std::memcpy(&items[static_cast<size_t>(pos) * 4], &lut.items[static_cast<size_t>(k) * 4], 16);
+    std::memcpy(&items[static_cast<size_t>(pos) * 4],
+                &lut.items[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4], 16);
   }
+}
+
+bool bsa::schedule_by_head(int64_t B, int64_t H, int64_t L, int64_t d, int dev) {
+  static int cache[64] = {0};
+  int l2 = (dev >= 0 && dev < 64) ? cache[dev] : 0;
+  if (l2 <= 0) {
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
+      return false;
+    if (dev >= 0 && dev < 64) cache[dev] = l2;
+  }
+  return B * H * L * d * 4 > static_cast<int64_t>(l2);
 }
 
 namespace {
@@ -125,6 +149,9 @@ void free_device(bsa_lut* lut) {
   if (lut->d_status) cudaFree(lut->d_status);
   if (lut->d_diag_pos) cudaFree(lut->d_diag_pos);
   if (lut->d_sched_start) cudaFree(lut->d_sched_start);
+  if (lut->d_items_g) cudaFree(lut->d_items_g);
+  if (lut->d_sched_start_g) cudaFree(lut->d_sched_start_g);
+  lut->d_items_g = lut->d_sched_start_g = nullptr;
   lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = lut->d_diag_pos = nullptr;
   lut->d_sched_start = nullptr;
   lut->device = -1;
@@ -221,12 +248,13 @@ int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32
   return BSA_OK;
 }
 
-int bsa_lut_schedule(const bsa_lut* lut, int grid, int32_t* items, int32_t* cta_start) {
+int bsa_lut_schedule(const bsa_lut* lut, int grid, int by_head, int32_t* items,
+                     int32_t* cta_start) {
   if (lut == nullptr) return BSA_ERR_NULL;
   if (grid < 1 || grid > std::max(1, lut->n_items)) return BSA_ERR_SHAPE;
   std::vector<int32_t> it, st;
   try {
-    bsa::build_schedule(*lut, grid, it, st);
+    bsa::build_schedule(*lut, grid, by_head != 0, it, st);
   } catch (const std::bad_alloc&) {
     return BSA_ERR_ALLOC;
   }
@@ -245,7 +273,8 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
   if (sms <= 0) return BSA_ERR_CUDA;
   lut->sched_grid = std::max(1, std::min(lut->n_items, sms));
   try {
-    bsa::build_schedule(*lut, lut->sched_grid, lut->sched_items, lut->sched_start);
+    for (int o = 0; o < 2; ++o)
+      bsa::build_schedule(*lut, lut->sched_grid, o == 1, lut->sched_items[o], lut->sched_start[o]);
   } catch (const std::bad_alloc&) {
     lut->sched_grid = 0;
     return BSA_ERR_ALLOC;
@@ -253,11 +282,13 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
   const size_t nr = lut->row_ptr.size() * 4;
   const size_t nc = std::max<size_t>(lut->col_idx.size(), 1) * 4;
   const size_t ni = std::max<size_t>(lut->items.size(), 4) * 4;
-  const size_t ns = lut->sched_start.size() * 4;
+  const size_t ns = lut->sched_start[0].size() * 4;
   if (cudaMalloc(&lut->d_row_ptr, nr) != cudaSuccess || cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess ||
       cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess ||
       cudaMalloc(&lut->d_diag_pos, lut->diag_pos.size() * 4) != cudaSuccess ||
-      cudaMalloc(&lut->d_sched_start, ns) != cudaSuccess) {
+      cudaMalloc(&lut->d_sched_start, ns) != cudaSuccess ||
+      cudaMalloc(&lut->d_items_g, ni) != cudaSuccess ||
+      cudaMalloc(&lut->d_sched_start_g, ns) != cudaSuccess) {
     free_device(lut);
     cudaGetLastError();
     return BSA_ERR_ALLOC;
@@ -267,11 +298,17 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
             (lut->col_idx.empty() ||
              cudaMemcpyAsync(lut->d_col_idx, lut->col_idx.data(), lut->col_idx.size() * 4,
                              cudaMemcpyHostToDevice, st) == cudaSuccess) &&
-            (lut->sched_items.empty() ||
-             cudaMemcpyAsync(lut->d_items, lut->sched_items.data(), lut->sched_items.size() * 4,
-                             cudaMemcpyHostToDevice, st) == cudaSuccess) &&
-            cudaMemcpyAsync(lut->d_sched_start, lut->sched_start.data(), ns, cudaMemcpyHostToDevice,
-                            st) == cudaSuccess &&
+            (lut->sched_items[0].empty() ||
+             (cudaMemcpyAsync(lut->d_items, lut->sched_items[0].data(),
+                              lut->sched_items[0].size() * 4, cudaMemcpyHostToDevice,
+                              st) == cudaSuccess &&
+              cudaMemcpyAsync(lut->d_items_g, lut->sched_items[1].data(),
+                              lut->sched_items[1].size() * 4, cudaMemcpyHostToDevice,
+                              st) == cudaSuccess)) &&
+            cudaMemcpyAsync(lut->d_sched_start, lut->sched_start[0].data(), ns,
+                            cudaMemcpyHostToDevice, st) == cudaSuccess &&
+            cudaMemcpyAsync(lut->d_sched_start_g, lut->sched_start[1].data(), ns,
+                            cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemcpyAsync(lut->d_diag_pos, lut->diag_pos.data(), lut->diag_pos.size() * 4,
                             cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
@@ -319,8 +356,9 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
     return BSA_ERR_CUDA;
 
   bsa::FwdParams p{};
-  p.items = reinterpret_cast<const int4*>(lut->d_items);
-  p.cta_start = lut->d_sched_start;
+  const bool by_head = bsa::schedule_by_head(B, H, L, d, dev);
+  p.items = reinterpret_cast<const int4*>(by_head ? lut->d_items_g : lut->d_items);
+  p.cta_start = by_head ? lut->d_sched_start_g : lut->d_sched_start;
   p.row_ptr = lut->d_row_ptr;
   p.col_idx = lut->d_col_idx;
   p.diag_pos = lut->d_diag_pos;

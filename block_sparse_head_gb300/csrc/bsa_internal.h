@@ -15,11 +15,12 @@ struct bsa_lut {
   std::vector<int32_t> col_idx;  // [nnz_total]
   std::vector<int32_t> items;    // [n_items][4] = {b, h, i, nnz}
   std::vector<int32_t> diag_pos; // [H*nb]: index of block i in row (h, i), or -1
-  // Device schedule for `sched_grid` CTAs (built at upload): the work list regrouped
-  // so that CTA c takes sched_items[sched_start[c] .. sched_start[c+1]).
+  // Device schedules for `sched_grid` CTAs (built at upload): the work list regrouped
+  // so that CTA c takes sched_items[o][sched_start[o][c] .. sched_start[o][c+1]).  o = 0
+  // hands items out in work-list order, o = 1 (batch, head) by (batch, head).
   int sched_grid = 0;
-  std::vector<int32_t> sched_items;  // [n_items][4]
-  std::vector<int32_t> sched_start;  // [sched_grid + 1]
+  std::vector<int32_t> sched_items[2];  // [n_items][4]
+  std::vector<int32_t> sched_start[2];  // [sched_grid + 1]
   // device copies (valid after bsa_lut_upload)
   int device = -1;
   int32_t* d_row_ptr = nullptr;
@@ -27,7 +28,9 @@ struct bsa_lut {
   int32_t* d_items = nullptr;
   int32_t* d_diag_pos = nullptr;
   int32_t* d_status = nullptr;
-  int32_t* d_sched_start = nullptr;  // device copy of sched_start (d_items holds sched_items)
+  int32_t* d_sched_start = nullptr;  // device copy of sched_start[0] (d_items: sched_items[0])
+  int32_t* d_items_g = nullptr;        // sched_items[1]
+  int32_t* d_sched_start_g = nullptr;  // sched_start[1]
   uint64_t wait_limit_ns = 10000000000ull;
 };
 
@@ -64,8 +67,13 @@ enum WaitSite : int {
 };
 
 // Regroups lut's work list for `grid` CTAs: CTA c takes items[start[c] .. start[c+1]).
-void build_schedule(const bsa_lut& lut, int grid, std::vector<int32_t>& items,
+// by_head: hand the items out (batch, head) by (batch, head) instead of in list order.
+void build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                     std::vector<int32_t>& start);
+
+// Whether a forward over [B,H,L,d] should use the (batch, head) schedule: its K and V
+// (B*H*L*d*4 bytes) exceed the L2 of device `dev`.
+bool schedule_by_head(int64_t B, int64_t H, int64_t L, int64_t d, int dev);
 
 // One launcher per supported (block, head_dim) pair; each lives in its own
 // translation unit so the variants compile in parallel.

@@ -108,12 +108,13 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   const int grid = std::max(1, std::min({lut->n_items, sms, kMaxGrid}));
   // The schedule made at upload serves when it was made for this grid; otherwise it is
   // built here (host memory only).
+  const int o = bsa::schedule_by_head(B, H, L, d, dev) ? 1 : 0;
   std::vector<int32_t> own_items, own_start;
-  const std::vector<int32_t>* sched_items = &lut->sched_items;
-  const std::vector<int32_t>* sched_start = &lut->sched_start;
-  if (lut->sched_grid != grid || lut->sched_start.empty()) {
+  const std::vector<int32_t>* sched_items = &lut->sched_items[o];
+  const std::vector<int32_t>* sched_start = &lut->sched_start[o];
+  if (lut->sched_grid != grid || lut->sched_start[o].empty()) {
     try {
-      bsa::build_schedule(*lut, grid, own_items, own_start);
+      bsa::build_schedule(*lut, grid, o == 1, own_items, own_start);
     } catch (const std::bad_alloc&) {
       return BSA_ERR_ALLOC;
     }

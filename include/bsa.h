@@ -102,21 +102,26 @@ int bsa_lut_info(const bsa_lut* lut, int* H, int* nb, int* batch, int* nnz_total
 int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32_t* items);
 
 /*
- * bsa_lut_schedule -- the per-CTA schedule the kernel runs for a grid of `grid` CTAs
- * (host only; needs no GPU).  The work list is handed out in its own order, each item
- * to the CTA with the least work so far (ties: lowest index), an item costing
- * 4*nnz + 2; CTA c then runs items[4*cta_start[c] .. 4*cta_start[c+1]) in the order it
- * received them.  items: 4*n_items int32, cta_start: grid+1 int32 (either may be NULL).
- * bsa_lut_upload uploads this schedule for grid = min(n_items, SM count).
+ * bsa_lut_schedule -- a per-CTA schedule the kernel runs for a grid of `grid` CTAs
+ * (host only; needs no GPU).  Items are handed out one at a time, each to the CTA with
+ * the least work so far (ties: lowest index), an item costing 4*nnz + 2; CTA c then runs
+ * items[4*cta_start[c] .. 4*cta_start[c+1]) in the order it received them.  by_head = 0
+ * hands them out in work-list order; nonzero, (batch, head) by (batch, head) (ascending),
+ * in work-list order within each pair.  items: 4*n_items int32, cta_start: grid+1 int32
+ * (either may be NULL).  bsa_lut_upload uploads both schedules for grid = min(n_items,
+ * SM count); bsa_forward runs the (batch, head) one when the K and V of the call
+ * (B*H*L*d*4 bytes) exceed the device's L2, so that the CTAs share a few pairs' K and V
+ * at a time, and the other one otherwise.
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE (grid < 1 or grid > max(1, n_items)),
  * BSA_ERR_ALLOC.
  */
-int bsa_lut_schedule(const bsa_lut* lut, int grid, int32_t* items, int32_t* cta_start);
+int bsa_lut_schedule(const bsa_lut* lut, int grid, int by_head, int32_t* items,
+                     int32_t* cta_start);
 
 /*
  * bsa_lut_upload -- allocate device copies of row_ptr, col_idx and the work list
  * (plus a device status word) on the current device and copy them there on
- * `stream`, then synchronize `stream`.  The device work list is the schedule of
+ * `stream`, then synchronize `stream`.  The device work lists are the two schedules of
  * bsa_lut_schedule for a grid of min(n_items, SM count of the device); the exported
  * list keeps its own order.  Call once before the first bsa_forward;
  * calling again re-uploads to the now-current device.  Errors: BSA_ERR_NULL,

@@ -129,10 +129,13 @@ def test_forward_validation_before_device_work(lib):
     assert lib.bsa_lut_info(None, None, None, None, None, None) == -1
 
 
-def _check_schedule(lut, grid):
+def _check_schedule(lut, grid, by_head=False):
     _, _, items = lut.export()
-    sched, start = lut.schedule(grid)
+    sched, start = lut.schedule(grid, by_head)
     n = lut.n_items
+    if by_head:  # hand-out order: (batch, head) ascending, list order inside each pair
+        order = sorted(range(n), key=lambda k: (items[k, 0], items[k, 1], k))
+        items = items[order]
     assert start[0] == 0 and start[-1] == n and np.all(np.diff(start) >= 0)
     # every work-list item exactly once; within a CTA in work-list order
     key = {tuple(r): k for k, r in enumerate(items.tolist())}
@@ -159,7 +162,8 @@ def test_schedule_workloads(lib, index):
     wl = wls.WORKLOADS[index]
     lut = binding.Lut(wls.layout_for(wl), wl.B)
     for grid in (1, 7, 152, lut.n_items):
-        _check_schedule(lut, min(grid, lut.n_items))
+        for by_head in (False, True):
+            _check_schedule(lut, min(grid, lut.n_items), by_head)
 
 
 @pytest.mark.parametrize("seed", range(4))
@@ -170,7 +174,8 @@ def test_schedule_random_and_errors(lib, seed):
                             empty_rows=int(rng.integers(0, nb + 1)))
     lut = binding.Lut(lay, B)
     for grid in sorted({1, 2, 5, lut.n_items}):
-        _check_schedule(lut, grid)
+        for by_head in (False, True):
+            _check_schedule(lut, grid, by_head)
     for bad in (0, -1, lut.n_items + 1):
         with pytest.raises(binding.BsaError):
             lut.schedule(bad)
