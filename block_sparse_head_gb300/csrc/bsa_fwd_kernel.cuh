@@ -71,7 +71,10 @@ struct FwdCfg {
   // Q tiles: two when they fit beside the K/V tiles, else one (b = 128, d = 128).
   static constexpr int kNQ = 2;
   static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
-  static constexpr int kKVRegion = kKR * 128;     // one 64-column box of a step tile
+  // A K or V step tile holds its blocks one after another, each as d/64 swizzled
+  // [b][64] column halves (the layout one 3-D TMA copy of a block lands in).
+  static constexpr int kHalfB = BLK * 128;        // one 64-column half of one block
+  static constexpr int kBlkB = BLK * D * 2;       // one block
   static constexpr int kOCol = kNS * 128;         // O after the S buffers
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
@@ -262,18 +265,10 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       const uint32_t fb = bar(C::kBarKF + t % 3);
       mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * BLK * D * 2);
       ++nk;
-      // One copy per tile with all column halves (K and V of 64-row blocks: one per half).
+      // One copy per tile or block, all column halves at once.
       if (first) tma_load_3d(sbase + C::kOffQ + qb * C::kQTile, tm_q, fb, 0, qrow, 0);
       const uint32_t kdst = sbase + C::kOffK + (t % 3) * C::kKVTile;
-      if (BLK == 128) {
-        tma_load_3d(kdst, tm_k, fb, 0, r0.krow[0], 0);
-      } else {
-        for (int g = 0; g < r0.nblk; ++g) {
-#pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc)
-            tma_load_3d(kdst + cc * C::kKVRegion + g * BLK * 128, tm_k, fb, 0, r0.krow[g], cc);
-        }
-      }
+      for (int g = 0; g < r0.nblk; ++g) tma_load_3d(kdst + g * C::kBlkB, tm_k, fb, 0, r0.krow[g], 0);
     }
     const StepRows rv = h2;
     if (rv.nblk > 0) {
@@ -287,15 +282,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
       ++nv;
       const uint32_t vdst = sbase + C::kOffV + (g % C::kNV) * C::kKVTile;
-      if (BLK == 128) {
-        tma_load_3d(vdst, tm_v, fb, 0, rv.krow[0], 0);
-      } else {
-        for (int b = 0; b < rv.nblk; ++b) {
-#pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc)
-            tma_load_3d(vdst + cc * C::kKVRegion + b * BLK * 128, tm_v, fb, 0, rv.krow[b], cc);
-        }
-      }
+      for (int b = 0; b < rv.nblk; ++b) tma_load_3d(vdst + b * C::kBlkB, tm_v, fb, 0, rv.krow[b], 0);
     }
     h2 = h1;
     h1 = r0;
@@ -320,7 +307,7 @@ struct MmaDescs {
     const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);
     hi = static_cast<uint32_t>(kdesc0 >> 32);
     k0 = static_cast<uint32_t>(kdesc0);
-    v0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffV, C::kKVRegion, 1024));
+    v0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffV, C::kHalfB, 1024));
     q0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffQ, 16, 1024));
   }
 };
@@ -347,12 +334,22 @@ __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, ui
     const uint32_t sb = tmem + (t % 3) * 128;
     const uint32_t qlo = md.q0 + qb * (C::kQTile >> 4);
     const uint32_t klo = md.k0 + (t % 3) * kTileStep;
-    const uint32_t idesc = (nblk == G) ? C::kIdescS : C::kIdescS1;
+    // b = 128: one N = 128 MMA per 16 columns of d.  b = 64: one N = 64 MMA per block
+    // (the blocks' rows are not contiguous), into S columns [64g, 64g + 64).
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      tc_mma_ss_lh(sb, qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4), md.hi,
-                   klo + (((kk >> 2) * C::kKVRegion + (kk & 3) * 32) >> 4), md.hi, idesc,
-                   kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t qa = qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4);
+      const uint32_t kb = klo + (((kk >> 2) * C::kHalfB + (kk & 3) * 32) >> 4);
+      if (BLK == 128) {
+        tc_mma_ss_lh(sb, qa, md.hi, kb, md.hi, C::kIdescS, kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < nblk)
+            tc_mma_ss_lh(sb + g * BLK, qa, md.hi, kb + ((g * C::kBlkB) >> 4), md.hi, C::kIdescS1,
+                         kk > 0 ? 1u : 0u);
+      }
+    }
     tc_commit(bar(C::kBarSF + t % 3));
   }
   // Let every MMA this thread issued finish before TMEM is released.
@@ -387,7 +384,9 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
 #pragma unroll
     for (int kk = 1; kk < C::kKR / 16; ++kk)
       if (kk < ksteps)
-        tc_mma_ts_lh(od, ps + kk * 8, vlo + kk * ((16 * 128) >> 4), md.hi, C::kIdescPV, 1u);
+        tc_mma_ts_lh(od, ps + kk * 8,
+                     vlo + ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4), md.hi,
+                     C::kIdescPV, 1u);
     tc_commit(bar(C::kBarPVD + g % 3));
   }
   tc_commit(bar(C::kBarDrainP));

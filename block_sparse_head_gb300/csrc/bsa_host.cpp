@@ -347,12 +347,8 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   if (dev != lut->device) return BSA_ERR_STATE;
 
   CUtensorMap tq, tk, tv;
-  // K and V of 64-row blocks go one half at a time: a step tile keeps each half's 128
-  // key rows (two blocks) together.
-  const int kv_halves = (block == 128) ? d / 64 : 1;
-  if (!encode_rows(&tq, q, rows, d, block, d / 64) ||
-      !encode_rows(&tk, k, rows, d, block, kv_halves) ||
-      !encode_rows(&tv, v, rows, d, block, kv_halves))
+  if (!encode_rows(&tq, q, rows, d, block, d / 64) || !encode_rows(&tk, k, rows, d, block, d / 64) ||
+      !encode_rows(&tv, v, rows, d, block, d / 64))
     return BSA_ERR_CUDA;
 
   bsa::FwdParams p{};

@@ -123,10 +123,9 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   }
 
   CUtensorMap tq, tk, tv;
-  const int kv_halves = (block == 128) ? d / 64 : 1;
   if (!encode_rows_noalloc(&tq, q, rows, d, block, d / 64) ||
-      !encode_rows_noalloc(&tk, k, rows, d, block, kv_halves) ||
-      !encode_rows_noalloc(&tv, v, rows, d, block, kv_halves))
+      !encode_rows_noalloc(&tk, k, rows, d, block, d / 64) ||
+      !encode_rows_noalloc(&tv, v, rows, d, block, d / 64))
     return BSA_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
