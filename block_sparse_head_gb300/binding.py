@@ -27,7 +27,8 @@ BSA_ERR_DEVICE_TIMEOUT = -8
 EXPORTED = (
     "bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule", "bsa_lut_upload",
     "bsa_lut_free",
-    "bsa_forward", "bsa_device_status", "bsa_set_wait_limit", "bsa_wait_selftest",
+    "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
+    "bsa_wait_selftest",
     "bsa_status_string", "bsa_version", "bsa_forward_noalloc",
 )
 
@@ -78,6 +79,7 @@ def load_library():
         lib.bsa_forward_noalloc.restype = ctypes.c_int
         lib.bsa_device_status.argtypes = [vp, vp, i32p]
         lib.bsa_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        lib.bsa_set_schedule.argtypes = [vp, ctypes.c_int]
         lib.bsa_wait_selftest.argtypes = [ctypes.c_uint64, vp]
         lib.bsa_status_string.argtypes = [ctypes.c_int]
         lib.bsa_status_string.restype = ctypes.c_char_p
@@ -85,7 +87,7 @@ def load_library():
         lib.bsa_version.restype = ctypes.c_char_p
         for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule",
                      "bsa_lut_upload",
-                     "bsa_forward", "bsa_device_status", "bsa_set_wait_limit",
+                     "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
                      "bsa_wait_selftest"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -146,6 +148,12 @@ class Lut:
         _check(self._lib.bsa_lut_upload(self.handle, _stream_handle(stream)), "bsa_lut_upload")
         self.device = torch.cuda.current_device()
         return self
+
+    _SCHEDULES = {"auto": 0, "list": 1, "by_head": 2}
+
+    def set_schedule(self, policy: str = "auto"):
+        """Device schedule of later forwards: "auto", "list" or "by_head"."""
+        _check(self._lib.bsa_set_schedule(self.handle, self._SCHEDULES[policy]), "bsa_set_schedule")
 
     def set_wait_limit(self, ns: int):
         _check(self._lib.bsa_set_wait_limit(self.handle, int(ns)), "bsa_set_wait_limit")

@@ -10,11 +10,13 @@
 //
 // Keys are consumed in steps of 128 rows: one block when b = 128, the next two active
 // blocks of the row when b = 64 (the last step of a row with an odd count holds one).
-// A CTA walks its share of the work list as one continuous stream of steps g = 0, 1, ...
+// A CTA walks its own range of the work list, regrouped per CTA on the host (each item to
+// the least-loaded CTA), as one continuous stream of steps g = 0, 1, ...
 //
 // GB300 mapping.  One CTA per SM, warp-specialised:
 //   warp 0      TMA producer.  For step t it loads K(t) (plus the Q tile when t opens an
-//               item) on one barrier and V(t-2) on another.
+//               item) on one barrier and V(t-2) on another; one 3-D copy per tile or
+//               block brings all of its column halves.
 //   warp 1      S issuer (one thread) and TMEM owner.  TMEM holds three S buffers and one
 //               O accumulator.  Step t: S(t) = Q K(t)^T into S[t % 3] once K(t) landed
 //               and PV(t-3), the last reader of that buffer, completed.
@@ -27,7 +29,8 @@
 //               quadrant, lane t and t+16 holding the two 64-key halves of one row.
 //               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
 //               lane t and t+16 holding the step's two key blocks.  Per step: TMEM ->
-//               registers, causal mask on diagonal blocks, base-2 online softmax (row max
+//               registers (the S barrier of the next step is probed during this one),
+//               causal mask on diagonal blocks, base-2 online softmax (row max
 //               by three-input maxima and one shuffle, exp2(s*c - m) with the scale c =
 //               scale*log2(e) folded into a packed f32x2 FFMA), lazy rescale (the
 //               running max moves only when it grows by more than 2^8), P -> TMEM as bf16

@@ -129,7 +129,9 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector
   }
 }
 
-bool bsa::schedule_by_head(int64_t B, int64_t H, int64_t L, int64_t d, int dev) {
+bool bsa::schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t d, int dev) {
+  if (policy == BSA_SCHEDULE_LIST) return false;
+  if (policy == BSA_SCHEDULE_BY_HEAD) return true;
   static int cache[64] = {0};
   int l2 = (dev >= 0 && dev < 64) ? cache[dev] : 0;
   if (l2 <= 0) {
@@ -352,7 +354,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
     return BSA_ERR_CUDA;
 
   bsa::FwdParams p{};
-  const bool by_head = bsa::schedule_by_head(B, H, L, d, dev);
+  const bool by_head = bsa::schedule_by_head(lut->sched_policy, B, H, L, d, dev);
   p.items = reinterpret_cast<const int4*>(by_head ? lut->d_items_g : lut->d_items);
   p.cta_start = by_head ? lut->d_sched_start_g : lut->d_sched_start;
   p.row_ptr = lut->d_row_ptr;
@@ -396,6 +398,14 @@ int bsa_device_status(const bsa_lut* lut, void* stream, int32_t* detail) {
     return BSA_ERR_CUDA;
   if (detail) *detail = word;
   return word == 0 ? BSA_OK : BSA_ERR_DEVICE_TIMEOUT;
+}
+
+int bsa_set_schedule(bsa_lut* lut, int policy) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (policy != BSA_SCHEDULE_AUTO && policy != BSA_SCHEDULE_LIST && policy != BSA_SCHEDULE_BY_HEAD)
+    return BSA_ERR_UNSUPPORTED;
+  lut->sched_policy = policy;
+  return BSA_OK;
 }
 
 int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns) {

@@ -19,6 +19,7 @@ struct bsa_lut {
   // so that CTA c takes sched_items[o][sched_start[o][c] .. sched_start[o][c+1]).  o = 0
   // hands items out in work-list order, o = 1 (batch, head) by (batch, head).
   int sched_grid = 0;
+  int sched_policy = 0;  // BSA_SCHEDULE_*
   std::vector<int32_t> sched_items[2];  // [n_items][4]
   std::vector<int32_t> sched_start[2];  // [sched_grid + 1]
   // device copies (valid after bsa_lut_upload)
@@ -71,9 +72,10 @@ enum WaitSite : int {
 void build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                     std::vector<int32_t>& start);
 
-// Whether a forward over [B,H,L,d] should use the (batch, head) schedule: its K and V
-// (B*H*L*d*4 bytes) exceed the L2 of device `dev`.
-bool schedule_by_head(int64_t B, int64_t H, int64_t L, int64_t d, int dev);
+// Whether a forward over [B,H,L,d] should use the (batch, head) schedule: as `policy`
+// says, or (BSA_SCHEDULE_AUTO) when its K and V (B*H*L*d*4 bytes) exceed the L2 of
+// device `dev`.
+bool schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t d, int dev);
 
 // One launcher per supported (block, head_dim) pair; each lives in its own
 // translation unit so the variants compile in parallel.

@@ -108,7 +108,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   const int grid = std::max(1, std::min({lut->n_items, sms, kMaxGrid}));
   // The schedule made at upload serves when it was made for this grid; otherwise it is
   // built here (host memory only).
-  const int o = bsa::schedule_by_head(B, H, L, d, dev) ? 1 : 0;
+  const int o = bsa::schedule_by_head(lut->sched_policy, B, H, L, d, dev) ? 1 : 0;
   std::vector<int32_t> own_items, own_start;
   const std::vector<int32_t>* sched_items = &lut->sched_items[o];
   const std::vector<int32_t>* sched_start = &lut->sched_start[o];

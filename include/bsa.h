@@ -111,7 +111,7 @@ int bsa_lut_export(const bsa_lut* lut, int32_t* row_ptr, int32_t* col_idx, int32
  * (either may be NULL).  bsa_lut_upload uploads both schedules for grid = min(n_items,
  * SM count); bsa_forward runs the (batch, head) one when the K and V of the call
  * (B*H*L*d*4 bytes) exceed the device's L2, so that the CTAs share a few pairs' K and V
- * at a time, and the other one otherwise.
+ * at a time, and the other one otherwise (bsa_set_schedule overrides the choice).
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE (grid < 1 or grid > max(1, n_items)),
  * BSA_ERR_ALLOC.
  */
@@ -196,6 +196,22 @@ int bsa_forward_noalloc(const void* q, const void* k, const void* v, const bsa_l
  * receives the raw status word: wait-site id in the low 16 bits.
  */
 int bsa_device_status(const bsa_lut* lut, void* stream, int32_t* detail);
+
+/* Device schedule policies (bsa_set_schedule). */
+enum {
+  BSA_SCHEDULE_AUTO = 0,    /* (batch, head) schedule when the call's K and V exceed L2 */
+  BSA_SCHEDULE_LIST = 1,    /* items handed out in work-list order */
+  BSA_SCHEDULE_BY_HEAD = 2  /* items handed out (batch, head) by (batch, head) */
+};
+
+/*
+ * bsa_set_schedule -- which of the two uploaded per-CTA schedules (bsa_lut_schedule)
+ * forwards queued after this call run: BSA_SCHEDULE_AUTO (default) picks the (batch,
+ * head) one when B*H*L*d*4 bytes of K and V exceed the device L2.  The schedule changes
+ * only the order in which CTAs take items; results are bitwise the same.  Errors:
+ * BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (unknown policy).
+ */
+int bsa_set_schedule(bsa_lut* lut, int policy);
 
 /*
  * bsa_set_wait_limit -- per-wait time limit, in nanoseconds, that kernels queued

@@ -168,6 +168,24 @@ def test_orders_agree_bitwise_and_deterministic():
     assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
 
 
+@pytest.mark.parametrize("index", [2, 3])
+def test_schedules_agree_bitwise(index):
+    """The two device schedules (work-list order, (batch, head) by (batch, head)) only
+    reorder whole items across CTAs: outputs are bitwise the same, and the same as the
+    automatic choice."""
+    wl = wls.WORKLOADS[index]
+    q, k, v = (t.cuda() for t in wls.qkv(wl))
+    lut = bsa.build_lut(wls.layout_for(wl), wl.B)
+    res = []
+    for policy in ("list", "by_head", "auto"):
+        lut.set_schedule(policy)
+        o, lse = bsa.forward(q, k, v, lut, wl.scale, wl.block, wl.causal_diag)
+        assert lut.device_status()[0] == 0
+        res.append((o.clone(), lse.clone()))
+    for o, lse in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(lse, res[0][1])
+
+
 def test_side_stream_and_guard_regions():
     """Runs on a non-default stream; output and lse guard regions stay untouched."""
     block, d, nb, B, H = 64, 128, 5, 2, 2

@@ -179,3 +179,11 @@ def test_schedule_random_and_errors(lib, seed):
     for bad in (0, -1, lut.n_items + 1):
         with pytest.raises(binding.BsaError):
             lut.schedule(bad)
+
+
+def test_schedule_policy_validation(lib):
+    lut = binding.Lut(np.ones((1, 2, 2), np.int32), 1)
+    for policy in ("auto", "list", "by_head"):
+        lut.set_schedule(policy)
+    assert lib.bsa_set_schedule(lut.handle, 3) == -6   # BSA_ERR_UNSUPPORTED
+    assert lib.bsa_set_schedule(None, 0) == -1         # BSA_ERR_NULL
