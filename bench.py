@@ -267,26 +267,50 @@ def gpu_arm(args) -> None:
         raise RuntimeError(f"device status {st} ({word:#x}) in the timed region")
 
     # e2e: host (pinned) buffers through the same C-ABI call, copies inside the region.
+    # Each step copies its q, k, v in, runs the forward and copies out, lse back.  Steps
+    # alternate between two streams, each with its own device buffers and LUT, so one
+    # step's copies overlap the neighbouring steps' forward and copies (as a serving loop
+    # would run); the serial figure (one stream, one step at a time) is reported beside it.
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    oh = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-    lh = torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True)
-    bufs = (qd, kd, vd, out, lse)
-    for _ in range(2):
-        binding.forward_host(qh, kh, vh, lut, wl.scale, wl.block, wl.causal_diag, out=oh, lse=lh,
-                             dev_bufs=bufs, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        binding.forward_host(qh, kh, vh, lut, wl.scale, wl.block, wl.causal_diag, out=oh, lse=lh,
-                             dev_bufs=bufs, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms_local = e0.elapsed_time(e1)
+    slots = []
+    for i in range(2):
+        lut_i = lut if i == 0 else bsa.build_lut(lay, wl.B, args.order)
+        bufs_i = (qd, kd, vd, out, lse) if i == 0 else tuple(torch.empty_like(t) for t in (qd, kd, vd, out, lse))
+        outs_i = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True),
+                  torch.empty(q.shape[:3], dtype=torch.float32, pin_memory=True))
+        slots.append((lut_i, bufs_i, outs_i, stream if i == 0 else torch.cuda.Stream()))
+
+    def e2e_step(i, serial):
+        lut_i, bufs_i, (oh, lh), st_i = slots[0 if serial else i % 2]
+        binding.forward_host(qh, kh, vh, lut_i, wl.scale, wl.block, wl.causal_diag, out=oh, lse=lh,
+                             dev_bufs=bufs_i, stream=st_i)
+
+    def e2e_time(serial):
+        for i in range(2):
+            e2e_step(i, serial)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0.record(slots[0][3])
+        slots[1][3].wait_event(e0)
+        for i in range(e2e_steps):
+            e2e_step(i, serial)
+        done = torch.cuda.Event()
+        done.record(slots[1][3])
+        slots[0][3].wait_event(done)
+        e1.record(slots[0][3])
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    e2e_serial_ms = e2e_time(True)
+    e2e_ms_local = e2e_time(False)
+    for lut_i, *_ in slots:
+        st, word = lut_i.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({word:#x}) in the e2e region")
 
     if pg:
         t = torch.tensor([local_ms, e2e_ms_local], device="cuda", dtype=torch.float64)
@@ -329,7 +353,10 @@ def gpu_arm(args) -> None:
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
                 "h2d_bytes_per_step": in_bytes,
                 "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
-                "steps": e2e_steps, "ms_per_step": round(e2e_ms / e2e_steps, 3)},
+                "steps": e2e_steps, "ms_per_step": round(e2e_ms / e2e_steps, 3),
+                "pipeline": "steps alternate over two streams (own buffers and LUT each)",
+                "serial_value": round(world * flops_step * e2e_steps / (e2e_serial_ms * 1e-3) / 1e12, 2),
+                "serial_ms_per_step": round(e2e_serial_ms / e2e_steps, 3)},
         "gpu_launches": args.steps,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 3),
