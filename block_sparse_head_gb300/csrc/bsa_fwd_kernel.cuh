@@ -124,31 +124,22 @@ __device__ __forceinline__ int step_blocks(int nnz, int s) {
   return rem < G ? rem : G;
 }
 
-// The CTA's share of the work list: items[cta_start[c] .. cta_start[c+1]) for CTA c.
-// Records are fetched two items ahead and each item's CSR row start and diagonal
-// position one item ahead of use.  A record with w = -1 marks the end.
+// The CTA's share of the work list: items[cta_start[c] .. cta_start[c+1]) for CTA c, as
+// device records {q_blk, kv_blk, rs, nnz | (dpos + 1) << 16}: the item's query block
+// among all B*H*nb (its rows start at q_blk * b), the first block of its (batch, head)'s
+// K and V (block j starts at row (kv_blk + j) * b), its row's first col_idx entry, its
+// active block count and the position of block i in its row (-1: none).  w = 0 marks an
+// empty item, w = -1 the end.  Records are fetched two items ahead of use.
 struct ItemStream {
   int t;                 // work-list index of the current item
   int end;               // one past the CTA's last item
   int n;                 // index of the current item among the non-empty ones
-  int4 cur;              // {b, h, i, nnz}
-  int cur_rs, cur_dp;    // first CSR entry of its row, position of block i in it (-1: none)
+  int4 cur;
   int4 nx1;
-  int nx1_rs, nx1_dp;
   int4 nx2;
 
   __device__ __forceinline__ int4 fetch(const FwdParams& p, int u) const {
     return u < end ? p.items[u] : make_int4(0, 0, 0, -1);
-  }
-  __device__ __forceinline__ static void fetch_aux(const FwdParams& p, const int4& r, int& rs,
-                                                   int& dp) {
-    rs = 0;
-    dp = -1;
-    if (r.w > 0) {
-      const int row = r.y * p.nb + r.z;
-      rs = p.row_ptr[row];
-      dp = p.diag_pos[row];
-    }
   }
   // Moves to the next item (kSkipEmpty: the next one with active blocks).
   template <bool kSkipEmpty>
@@ -156,10 +147,7 @@ struct ItemStream {
     for (;;) {
       ++t;
       cur = nx1;
-      cur_rs = nx1_rs;
-      cur_dp = nx1_dp;
       nx1 = nx2;
-      fetch_aux(p, nx1, nx1_rs, nx1_dp);
       nx2 = fetch(p, t + 2);
       if (cur.w > 0) ++n;
       if (!kSkipEmpty || cur.w != 0) return;
@@ -171,11 +159,12 @@ struct ItemStream {
     end = p.cta_start[blockIdx.x + 1];
     n = -1;
     nx1 = fetch(p, t + 1);
-    fetch_aux(p, nx1, nx1_rs, nx1_dp);
     nx2 = fetch(p, t + 2);
     next<kSkipEmpty>(p);
   }
   __device__ __forceinline__ bool done() const { return cur.w < 0; }
+  __device__ __forceinline__ int nnz() const { return cur.w & 0xFFFF; }
+  __device__ __forceinline__ int dpos() const { return (cur.w >> 16) - 1; }
 };
 
 // Steps of the non-empty items, in order.
@@ -186,17 +175,17 @@ struct StepCursor {
   __device__ __forceinline__ void init(const FwdParams& p) {
     is.init<true>(p);
     s = 0;
-    nsteps = is.done() ? 0 : (is.cur.w + G - 1) / G;
+    nsteps = is.done() ? 0 : (is.nnz() + G - 1) / G;
   }
   __device__ __forceinline__ void advance(const FwdParams& p) {
     if (++s >= nsteps) {
       is.next<true>(p);
       s = 0;
-      nsteps = is.done() ? 0 : (is.cur.w + G - 1) / G;
+      nsteps = is.done() ? 0 : (is.nnz() + G - 1) / G;
     }
   }
   __device__ __forceinline__ bool valid() const { return !is.done(); }
-  __device__ __forceinline__ int nblk() const { return step_blocks<G>(is.cur.w, s); }
+  __device__ __forceinline__ int nblk() const { return step_blocks<G>(is.nnz(), s); }
 };
 
 // ----------------------------------------------------------------- producer
@@ -221,7 +210,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
   auto fetch_cols = [&]() {
     if (!c.valid()) return;
     const int nb = c.nblk();
-    const int* cols = p.col_idx + c.is.cur_rs + c.s * G;
+    const int* cols = p.col_idx + c.is.cur.z + c.s * G;
 #pragma unroll
     for (int g = 0; g < G; ++g) colv[g] = (g < nb) ? cols[g] : 0;
   };
@@ -238,15 +227,14 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
     int qrow = 0, qb = 0;
     if (c.valid()) {
       r0.nblk = c.nblk();
-      const int rowbase = (c.is.cur.x * p.H + c.is.cur.y) * p.L;
 #pragma unroll
-      for (int g = 0; g < G; ++g) r0.krow[g] = rowbase + colv[g] * BLK;
+      for (int g = 0; g < G; ++g) r0.krow[g] = (c.is.cur.y + colv[g]) * BLK;
       first = (c.s == 0);
-      qrow = rowbase + c.is.cur.z * BLK;
+      qrow = c.is.cur.x * BLK;
       qb = c.is.n % C::kNQ;
       if (first && c.is.nx1.w > 0) {
         // Warm L2 with the following item's Q.
-        const int nrow = (c.is.nx1.x * p.H + c.is.nx1.y) * p.L + c.is.nx1.z * BLK;
+        const int nrow = c.is.nx1.x * BLK;
 #pragma unroll
         tma_prefetch_l2_3d(tm_q, 0, nrow, 0);
       }
@@ -271,7 +259,9 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       // One copy per tile or block, all column halves at once.
       if (first) tma_load_3d(sbase + C::kOffQ + qb * C::kQTile, tm_q, fb, 0, qrow, 0);
       const uint32_t kdst = sbase + C::kOffK + (t % 3) * C::kKVTile;
-      for (int g = 0; g < r0.nblk; ++g) tma_load_3d(kdst + g * C::kBlkB, tm_k, fb, 0, r0.krow[g], 0);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (g < r0.nblk) tma_load_3d(kdst + g * C::kBlkB, tm_k, fb, 0, r0.krow[g], 0);
     }
     const StepRows rv = h2;
     if (rv.nblk > 0) {
@@ -285,7 +275,9 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
       ++nv;
       const uint32_t vdst = sbase + C::kOffV + (g % C::kNV) * C::kKVTile;
-      for (int b = 0; b < rv.nblk; ++b) tma_load_3d(vdst + b * C::kBlkB, tm_v, fb, 0, rv.krow[b], 0);
+#pragma unroll
+      for (int b = 0; b < G; ++b)
+        if (b < rv.nblk) tma_load_3d(vdst + b * C::kBlkB, tm_v, fb, 0, rv.krow[b], 0);
     }
     h2 = h1;
     h1 = r0;
@@ -498,9 +490,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
 
   ItemStream is;
   for (is.init<false>(p); ok && !is.done(); is.next<false>(p)) {
-    const int4 it = is.cur;
-    const int nnz = it.w;
-    const int qrow = (it.x * p.H + it.y) * p.L + it.z * BLK + row;  // global query row
+    const int nnz = is.nnz();
+    const int qrow = is.cur.x * BLK + row;  // global query row
     if (nnz == 0) {
       uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
 #pragma unroll
@@ -508,7 +499,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       if (half == 0) p.lse[qrow] = -INFINITY;
       continue;
     }
-    const int dpos = p.causal_diag ? is.cur_dp : -1;  // position of block i in the row
+    const int dpos = p.causal_diag ? is.dpos() : -1;  // position of block i in the row
     const int nsteps = (nnz + G - 1) / G;
     float m_used = -INFINITY;
     float l = 0.f;

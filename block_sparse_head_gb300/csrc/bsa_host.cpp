@@ -129,6 +129,20 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector
   }
 }
 
+void bsa::device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
+                         std::vector<int32_t>& records) {
+  records.resize(items.size());
+  for (size_t k = 0; k + 3 < items.size(); k += 4) {
+    const int32_t b = items[k], h = items[k + 1], i = items[k + 2], nnz = items[k + 3];
+    const int32_t row = h * lut.nb + i;
+    const int32_t kv = (b * lut.H + h) * lut.nb;
+    records[k] = kv + i;
+    records[k + 1] = kv;
+    records[k + 2] = lut.row_ptr[static_cast<size_t>(row)];
+    records[k + 3] = nnz | ((lut.diag_pos[static_cast<size_t>(row)] + 1) << 16);
+  }
+}
+
 bool bsa::schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t d, int dev) {
   if (policy == BSA_SCHEDULE_LIST) return false;
   if (policy == BSA_SCHEDULE_BY_HEAD) return true;
@@ -145,16 +159,14 @@ bool bsa::schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t 
 namespace {
 
 void free_device(bsa_lut* lut) {
-  if (lut->d_row_ptr) cudaFree(lut->d_row_ptr);
   if (lut->d_col_idx) cudaFree(lut->d_col_idx);
   if (lut->d_items) cudaFree(lut->d_items);
   if (lut->d_status) cudaFree(lut->d_status);
-  if (lut->d_diag_pos) cudaFree(lut->d_diag_pos);
   if (lut->d_sched_start) cudaFree(lut->d_sched_start);
   if (lut->d_items_g) cudaFree(lut->d_items_g);
   if (lut->d_sched_start_g) cudaFree(lut->d_sched_start_g);
   lut->d_items_g = lut->d_sched_start_g = nullptr;
-  lut->d_row_ptr = lut->d_col_idx = lut->d_items = lut->d_status = lut->d_diag_pos = nullptr;
+  lut->d_col_idx = lut->d_items = lut->d_status = nullptr;
   lut->d_sched_start = nullptr;
   lut->device = -1;
 }
@@ -167,7 +179,9 @@ int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bs
   if (out == nullptr) return BSA_ERR_NULL;
   *out = nullptr;
   if (layout == nullptr) return BSA_ERR_NULL;
-  if (H < 1 || nb < 1 || batch < 1) return BSA_ERR_SHAPE;
+  // nb < 2^15: the device work-list record packs a row's count and diagonal position
+  // into 16 bits each.
+  if (H < 1 || nb < 1 || nb > 32767 || batch < 1) return BSA_ERR_SHAPE;
   const int64_t cells = static_cast<int64_t>(H) * nb * nb;
   const int64_t n_items = static_cast<int64_t>(batch) * H * nb;
   if (cells > kInt32Max || n_items > kInt32Max) return BSA_ERR_SHAPE;
@@ -274,20 +288,21 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
   const int sms = sm_count(dev);
   if (sms <= 0) return BSA_ERR_CUDA;
   lut->sched_grid = std::max(1, std::min(lut->n_items, sms));
+  std::vector<int32_t>* rec = lut->sched_records;  // device records of both schedules
   try {
-    for (int o = 0; o < 2; ++o)
+    for (int o = 0; o < 2; ++o) {
       bsa::build_schedule(*lut, lut->sched_grid, o == 1, lut->sched_items[o], lut->sched_start[o]);
+      bsa::device_records(*lut, lut->sched_items[o], rec[o]);
+    }
   } catch (const std::bad_alloc&) {
     lut->sched_grid = 0;
     return BSA_ERR_ALLOC;
   }
-  const size_t nr = lut->row_ptr.size() * 4;
   const size_t nc = std::max<size_t>(lut->col_idx.size(), 1) * 4;
   const size_t ni = std::max<size_t>(lut->items.size(), 4) * 4;
   const size_t ns = lut->sched_start[0].size() * 4;
-  if (cudaMalloc(&lut->d_row_ptr, nr) != cudaSuccess || cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess ||
-      cudaMalloc(&lut->d_items, ni) != cudaSuccess || cudaMalloc(&lut->d_status, 16) != cudaSuccess ||
-      cudaMalloc(&lut->d_diag_pos, lut->diag_pos.size() * 4) != cudaSuccess ||
+  if (cudaMalloc(&lut->d_col_idx, nc) != cudaSuccess || cudaMalloc(&lut->d_items, ni) != cudaSuccess ||
+      cudaMalloc(&lut->d_status, 16) != cudaSuccess ||
       cudaMalloc(&lut->d_sched_start, ns) != cudaSuccess ||
       cudaMalloc(&lut->d_items_g, ni) != cudaSuccess ||
       cudaMalloc(&lut->d_sched_start_g, ns) != cudaSuccess) {
@@ -295,23 +310,17 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
     cudaGetLastError();
     return BSA_ERR_ALLOC;
   }
-  bool ok = cudaMemcpyAsync(lut->d_row_ptr, lut->row_ptr.data(), nr, cudaMemcpyHostToDevice, st) ==
-                cudaSuccess &&
-            (lut->col_idx.empty() ||
+  bool ok = (lut->col_idx.empty() ||
              cudaMemcpyAsync(lut->d_col_idx, lut->col_idx.data(), lut->col_idx.size() * 4,
                              cudaMemcpyHostToDevice, st) == cudaSuccess) &&
-            (lut->sched_items[0].empty() ||
-             (cudaMemcpyAsync(lut->d_items, lut->sched_items[0].data(),
-                              lut->sched_items[0].size() * 4, cudaMemcpyHostToDevice,
-                              st) == cudaSuccess &&
-              cudaMemcpyAsync(lut->d_items_g, lut->sched_items[1].data(),
-                              lut->sched_items[1].size() * 4, cudaMemcpyHostToDevice,
-                              st) == cudaSuccess)) &&
+            (rec[0].empty() ||
+             (cudaMemcpyAsync(lut->d_items, rec[0].data(), rec[0].size() * 4,
+                              cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(lut->d_items_g, rec[1].data(), rec[1].size() * 4,
+                              cudaMemcpyHostToDevice, st) == cudaSuccess)) &&
             cudaMemcpyAsync(lut->d_sched_start, lut->sched_start[0].data(), ns,
                             cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemcpyAsync(lut->d_sched_start_g, lut->sched_start[1].data(), ns,
-                            cudaMemcpyHostToDevice, st) == cudaSuccess &&
-            cudaMemcpyAsync(lut->d_diag_pos, lut->diag_pos.data(), lut->diag_pos.size() * 4,
                             cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
             cudaStreamSynchronize(st) == cudaSuccess;
@@ -357,9 +366,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   const bool by_head = bsa::schedule_by_head(lut->sched_policy, B, H, L, d, dev);
   p.items = reinterpret_cast<const int4*>(by_head ? lut->d_items_g : lut->d_items);
   p.cta_start = by_head ? lut->d_sched_start_g : lut->d_sched_start;
-  p.row_ptr = lut->d_row_ptr;
   p.col_idx = lut->d_col_idx;
-  p.diag_pos = lut->d_diag_pos;
   p.out = out;
   p.lse = lse;
   p.status = lut->d_status;

@@ -22,15 +22,14 @@ struct bsa_lut {
   int sched_policy = 0;  // BSA_SCHEDULE_*
   std::vector<int32_t> sched_items[2];  // [n_items][4]
   std::vector<int32_t> sched_start[2];  // [sched_grid + 1]
+  std::vector<int32_t> sched_records[2];  // device records of sched_items (device_records)
   // device copies (valid after bsa_lut_upload)
   int device = -1;
-  int32_t* d_row_ptr = nullptr;
   int32_t* d_col_idx = nullptr;
   int32_t* d_items = nullptr;
-  int32_t* d_diag_pos = nullptr;
   int32_t* d_status = nullptr;
-  int32_t* d_sched_start = nullptr;  // device copy of sched_start[0] (d_items: sched_items[0])
-  int32_t* d_items_g = nullptr;        // sched_items[1]
+  int32_t* d_sched_start = nullptr;  // device copy of sched_start[0] (d_items: records of sched_items[0])
+  int32_t* d_items_g = nullptr;        // records of sched_items[1]
   int32_t* d_sched_start_g = nullptr;  // sched_start[1]
   uint64_t wait_limit_ns = 10000000000ull;
 };
@@ -39,11 +38,9 @@ namespace bsa {
 
 // Kernel arguments besides the three tensor maps.
 struct FwdParams {
-  const int4* items;        // work list {b, h, i, nnz}, regrouped per CTA
+  const int4* items;        // work list regrouped per CTA, as device records (kernel header)
   const int32_t* cta_start; // CTA c takes items[cta_start[c] .. cta_start[c+1])
-  const int32_t* row_ptr;   // CSR row starts over rows h*nb + i
   const int32_t* col_idx;   // active column blocks, ascending per row
-  const int32_t* diag_pos;  // per row h*nb + i: position of block i in the row, or -1
   void* out;                // bf16 [B,H,L,d]
   float* lse;               // fp32 [B,H,L]
   int32_t* status;          // device status word (0 = fine)
@@ -71,6 +68,13 @@ enum WaitSite : int {
 // by_head: hand the items out (batch, head) by (batch, head) instead of in list order.
 void build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                     std::vector<int32_t>& start);
+
+// Device records of a regrouped work list `items` ({b, h, i, nnz} each):
+// {q_blk, kv_blk, first col_idx entry of the row, nnz | (dpos + 1) << 16} with q_blk =
+// (b*H + h)*nb + i, kv_blk = (b*H + h)*nb and dpos the position of block i in row (h, i)
+// (-1 if absent), so the kernel needs no other table to start an item.
+void device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
+                    std::vector<int32_t>& records);
 
 // Whether a forward over [B,H,L,d] should use the (batch, head) schedule: as `policy`
 // says, or (BSA_SCHEDULE_AUTO) when its K and V (B*H*L*d*4 bytes) exceed the L2 of

@@ -35,9 +35,8 @@ constexpr int kMaxGrid = 1023;
 
 // Layout, in int32 words, each part starting on a 16-byte boundary:
 //   [0, 4)           status word (+ padding)
-//   [4, 4 + 4n)      work list, n items of {b, h, i, nnz}, regrouped per CTA
-//   then the per-CTA starts (grid + 1 words), row_ptr (H*nb + 1 words), diag_pos (H*nb
-//   words), col_idx (nnz words)
+//   [4, 4 + 4n)      work list regrouped per CTA, n device records of 4 words
+//   then the per-CTA starts (grid + 1 words) and col_idx (nnz words)
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 // Device address of g_noalloc_scratch per device, looked up once with that device
@@ -87,9 +86,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
 
   const size_t off_items = 4;
   const size_t off_start = off_items + round4(static_cast<size_t>(lut->n_items) * 4);
-  const size_t off_rowptr = off_start + round4(static_cast<size_t>(kMaxGrid) + 1);
-  const size_t off_diag = off_rowptr + round4(lut->row_ptr.size());
-  const size_t off_colidx = off_diag + round4(lut->diag_pos.size());
+  const size_t off_colidx = off_start + round4(static_cast<size_t>(kMaxGrid) + 1);
   const size_t total = off_colidx + round4(lut->col_idx.size());
   if (total > kNoAllocScratchWords) return BSA_ERR_TOO_LARGE;
 
@@ -109,16 +106,17 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   // The schedule made at upload serves when it was made for this grid; otherwise it is
   // built here (host memory only).
   const int o = bsa::schedule_by_head(lut->sched_policy, B, H, L, d, dev) ? 1 : 0;
-  std::vector<int32_t> own_items, own_start;
-  const std::vector<int32_t>* sched_items = &lut->sched_items[o];
+  std::vector<int32_t> own_items, own_start, own_records;
+  const std::vector<int32_t>* sched_items = &lut->sched_records[o];
   const std::vector<int32_t>* sched_start = &lut->sched_start[o];
   if (lut->sched_grid != grid || lut->sched_start[o].empty()) {
     try {
       bsa::build_schedule(*lut, grid, o == 1, own_items, own_start);
+      bsa::device_records(*lut, own_items, own_records);
     } catch (const std::bad_alloc&) {
       return BSA_ERR_ALLOC;
     }
-    sched_items = &own_items;
+    sched_items = &own_records;
     sched_start = &own_start;
   }
 
@@ -136,10 +134,6 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
                        cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       cudaMemcpyAsync(base + off_start, sched_start->data(), sched_start->size() * 4,
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(base + off_rowptr, lut->row_ptr.data(), lut->row_ptr.size() * 4,
-                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(base + off_diag, lut->diag_pos.data(), lut->diag_pos.size() * 4,
-                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
       (!lut->col_idx.empty() &&
        cudaMemcpyAsync(base + off_colidx, lut->col_idx.data(), lut->col_idx.size() * 4,
                        cudaMemcpyHostToDevice, st) != cudaSuccess))
@@ -148,9 +142,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   bsa::FwdParams p{};
   p.items = reinterpret_cast<const int4*>(base + off_items);
   p.cta_start = base + off_start;
-  p.row_ptr = base + off_rowptr;
   p.col_idx = base + off_colidx;
-  p.diag_pos = base + off_diag;
   p.out = out;
   p.lse = lse;
   p.status = base;

@@ -75,7 +75,7 @@ typedef struct bsa_lut bsa_lut;
  * section 3.2, "Implementation with Sparse Matrix Formats".
  *
  *   layout  host, int32 [H, nb, nb], values 0/1, row-major; read only, not retained.
- *   H, nb   heads and blocks per side (both >= 1; H*nb*nb < 2^31).
+ *   H, nb   heads and blocks per side (both >= 1, nb < 2^15, H*nb*nb < 2^31).
  *   batch   batch size B the work list is built for (>= 1).
  *   order   BSA_ORDER_GLOBAL or BSA_ORDER_GROUPED.
  *   out     receives the new LUT (set to NULL on error).
@@ -119,8 +119,8 @@ int bsa_lut_schedule(const bsa_lut* lut, int grid, int by_head, int32_t* items,
                      int32_t* cta_start);
 
 /*
- * bsa_lut_upload -- allocate device copies of row_ptr, col_idx and the work list
- * (plus a device status word) on the current device and copy them there on
+ * bsa_lut_upload -- allocate device copies of col_idx and the work list (plus a
+ * device status word) on the current device and copy them there on
  * `stream`, then synchronize `stream`.  The device work lists are the two schedules of
  * bsa_lut_schedule for a grid of min(n_items, SM count of the device); the exported
  * list keeps its own order.  Call once before the first bsa_forward;
@@ -175,8 +175,8 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
  *                call synchronizes `stream` after the kernel and returns
  *                BSA_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel gave up.
  *
- * Limit: 4 + 4*n_items + 1024 + (H*nb + 1) + H*nb + nnz int32 words (each part rounded
- * up to 4 words) must fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before
+ * Limit: 4 + 4*n_items + 1024 + nnz int32 words (each part rounded up to 4 words) must
+ * fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before
  * any device work.  The per-CTA schedule comes from bsa_lut_upload when the LUT was
  * uploaded on this device; otherwise the call builds it in host memory.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any

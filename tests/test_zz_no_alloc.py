@@ -82,7 +82,7 @@ def test_noalloc_matches_forward_two_calls(cuda_lib, name, B, block, d, causal, 
 
 def test_noalloc_rejects_oversized_lut(cuda_lib):
     lib = cuda_lib
-    # 1 x 1 x 1024 blocks of 64 -> 1024 items (4096 words) + row_ptr + 1024*1024 col_idx words
+    # 1 x 1 x 1024 blocks of 64 -> 1024 items (4096 words) + 1024*1024 col_idx words
     nb = 1024
     lay = torch.ones(1, nb, nb, dtype=torch.int32)
     lut = bsa.build_lut(lay, 1, upload=False)
