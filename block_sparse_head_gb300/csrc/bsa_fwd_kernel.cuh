@@ -38,8 +38,9 @@
 //               next item's first P is handed over, then normalised and stored as bf16
 //               with lse = ln 2 * (m + log2 l).  An item with no active block writes O = 0
 //               and lse = -inf.
-// Work-list records, CSR row starts and column indices are fetched one item / one step
-// ahead of use, so no role waits on a global load in its steady state.
+// Work-list records (which carry each item's block indices, CSR row start and diagonal
+// position) are fetched two items ahead and column indices one step ahead of use, so no
+// role waits on a global load in its steady state.
 //
 // Every barrier wait is bounded (WaitCtl): a wait that runs out records a timeout in
 // the status word, and all roles leave their loops, drain in-flight copies and MMAs,
