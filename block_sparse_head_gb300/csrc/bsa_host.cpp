@@ -370,10 +370,6 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   p.out = out;
   p.lse = lse;
   p.status = lut->d_status;
-  p.n_items = lut->n_items;
-  p.H = H;
-  p.L = L;
-  p.nb = lut->nb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;

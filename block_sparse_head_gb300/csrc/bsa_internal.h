@@ -44,8 +44,6 @@ struct FwdParams {
   void* out;                // bf16 [B,H,L,d]
   float* lse;               // fp32 [B,H,L]
   int32_t* status;          // device status word (0 = fine)
-  int n_items;
-  int H, L, nb;
   float scale_log2;         // scale * log2(e)
   int causal_diag;
   unsigned long long wait_limit_ns;

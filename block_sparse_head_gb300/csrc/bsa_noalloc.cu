@@ -146,10 +146,6 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   p.out = out;
   p.lse = lse;
   p.status = base;
-  p.n_items = lut->n_items;
-  p.H = H;
-  p.L = L;
-  p.nb = lut->nb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
