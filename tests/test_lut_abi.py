@@ -98,6 +98,9 @@ def test_build_lut_errors(lib):
     assert _build_status(lib, ones, 0, 2, 1)[0] == -2
     assert _build_status(lib, ones, 1, 0, 1)[0] == -2
     assert _build_status(lib, ones, 1, 2, 0)[0] == -2
+    # nb >= 2^15 is refused before the layout is read (the device records pack the row
+    # count and diagonal position into 16 bits each)
+    assert _build_status(lib, ones, 1, 32768, 1)[0] == -2
     assert _build_status(lib, ones, 1, 2, 1, order=7)[0] == -6
     bad = ones.copy()
     bad[0, 1, 0] = 2
