@@ -196,6 +196,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(values, pg, device="cuda") -> list:
+    """The slowest rank's value of each timing (ranks run weak-scaling replicas); the
+    values themselves on one rank.  `pg` is torch.distributed or None."""
+    if pg is None:
+        return [float(x) for x in values]
+    import torch
+
+    t = torch.tensor([float(x) for x in values], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_tflops(world: int, flops_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank does `steps` steps of `flops_per_step` in `ms`."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def workload_config(wl, l2_note: str, world: int) -> dict:
     return {"workload": f"{wl.name} (workload {wl.index})", "batch": wl.B, "heads": wl.H,
             "seq_len": wl.L, "block": wl.block, "head_dim": wl.d,
@@ -317,25 +334,20 @@ def gpu_arm(args) -> None:
         if st != 0:
             raise RuntimeError(f"device status {st} ({word:#x}) in the e2e region")
 
-    if pg:
-        t = torch.tensor([local_ms, e2e_ms_local], device="cuda", dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        local_ms, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = e2e_ms_local
+    local_ms, e2e_ms, e2e_serial_ms = max_over_ranks([local_ms, e2e_ms_local, e2e_serial_ms], pg)
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return
 
     ms_per_step = local_ms / args.steps
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, local_ms)
     peaks = measured_peaks()
     peak_kind = "bf16_burst" if local_ms < 3000 else "bf16_sustained"
     peak = peaks[peak_kind]
     achieved = flops_step / (statistics.mean(per_step_ms) * 1e-3) / 1e12
     traffic = recorded_traffic(wl.name)
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = job_tflops(world, flops_step, e2e_steps, e2e_ms)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -360,7 +372,7 @@ def gpu_arm(args) -> None:
                 "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
                 "steps": e2e_steps, "ms_per_step": round(e2e_ms / e2e_steps, 3),
                 "pipeline": "steps alternate over two streams (own buffers and LUT each)",
-                "serial_value": round(world * flops_step * e2e_steps / (e2e_serial_ms * 1e-3) / 1e12, 2),
+                "serial_value": round(job_tflops(world, flops_step, e2e_steps, e2e_serial_ms), 2),
                 "serial_ms_per_step": round(e2e_serial_ms / e2e_steps, 3)},
         "gpu_launches": args.steps,
         "clocks": clk,
