@@ -23,3 +23,19 @@ def cuda_lib():
     import block_sparse_head_gb300 as bsa
 
     return bsa.load_library()
+
+
+_PARITY_LINES: list[str] = []
+
+
+@pytest.fixture(scope="session")
+def parity_report():
+    """Lines of full-size parity figures, printed in the terminal summary."""
+    return _PARITY_LINES
+
+
+def pytest_terminal_summary(terminalreporter):
+    if _PARITY_LINES:
+        terminalreporter.write_sep("-", "full-size parity against the oracle")
+        for line in _PARITY_LINES:
+            terminalreporter.write_line(line)
