@@ -29,7 +29,7 @@ EXPORTED = (
     "bsa_lut_free",
     "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
     "bsa_wait_selftest",
-    "bsa_status_string", "bsa_version", "bsa_forward_noalloc",
+    "bsa_status_string", "bsa_version", "bsa_forward_noalloc", "bsa_debug_expire_wait",
 )
 
 _lib = None
@@ -80,6 +80,7 @@ def load_library():
         lib.bsa_device_status.argtypes = [vp, vp, i32p]
         lib.bsa_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
         lib.bsa_set_schedule.argtypes = [vp, ctypes.c_int]
+        lib.bsa_debug_expire_wait.argtypes = [vp, ctypes.c_int]
         lib.bsa_wait_selftest.argtypes = [ctypes.c_uint64, vp]
         lib.bsa_status_string.argtypes = [ctypes.c_int]
         lib.bsa_status_string.restype = ctypes.c_char_p
@@ -88,7 +89,7 @@ def load_library():
         for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule",
                      "bsa_lut_upload",
                      "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
-                     "bsa_wait_selftest"):
+                     "bsa_wait_selftest", "bsa_debug_expire_wait"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -157,6 +158,10 @@ class Lut:
 
     def set_wait_limit(self, ns: int):
         _check(self._lib.bsa_set_wait_limit(self.handle, int(ns)), "bsa_set_wait_limit")
+
+    def debug_expire_wait(self, site: int):
+        """Test knob: later forwards treat every wait at ``site`` as run out (0: off)."""
+        _check(self._lib.bsa_debug_expire_wait(self.handle, int(site)), "bsa_debug_expire_wait")
 
     def device_status(self, stream=None) -> tuple[int, int]:
         """(status, raw word) of the device status word; synchronizes the stream."""

@@ -99,6 +99,10 @@ struct FwdCfg {
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // Launch request: more than half of the SM's shared memory, so that two CTAs never
+  // share an SM (each allocates all 512 TMEM columns; a second one would stall in
+  // tcgen05.alloc until the first, persistent, CTA finished).
+  static constexpr int kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
   // instruction descriptors: S over a full step (N = 128) or a single 64-key block
   static constexpr uint32_t kIdescS = idesc_bf16_f32(BLK, kKR, false, false);
   static constexpr uint32_t kIdescS1 = idesc_bf16_f32(BLK, BLK, false, false);
@@ -679,7 +683,7 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
+  const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, p.expire_site};
 
   if (warp == 0) {
     if (lane == 0) fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
@@ -710,11 +714,11 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& q, const CUtensorM
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     e = cudaFuncSetAttribute(bsa_fwd_kernel<BLK, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+                             C::kLaunchSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  bsa_fwd_kernel<BLK, D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, p);
+  bsa_fwd_kernel<BLK, D><<<grid, C::kThreads, C::kLaunchSmem, stream>>>(q, k, v, p);
   return cudaGetLastError();
 }
 

@@ -373,6 +373,7 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
+  p.expire_site = lut->expire_site;
 
   const int grid = lut->sched_grid;  // the schedule uploaded with the LUT
   if (grid <= 0) return BSA_ERR_STATE;
@@ -414,6 +415,13 @@ int bsa_set_schedule(bsa_lut* lut, int policy) {
 int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns) {
   if (lut == nullptr) return BSA_ERR_NULL;
   lut->wait_limit_ns = ns == 0 ? 10000000000ull : ns;
+  return BSA_OK;
+}
+
+int bsa_debug_expire_wait(bsa_lut* lut, int site) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (site < 0 || site > 0xFFFF) return BSA_ERR_UNSUPPORTED;
+  lut->expire_site = site;
   return BSA_OK;
 }
 

@@ -32,6 +32,7 @@ struct bsa_lut {
   int32_t* d_items_g = nullptr;        // records of sched_items[1]
   int32_t* d_sched_start_g = nullptr;  // sched_start[1]
   uint64_t wait_limit_ns = 10000000000ull;
+  int expire_site = 0;  // bsa_debug_expire_wait
 };
 
 namespace bsa {
@@ -47,6 +48,7 @@ struct FwdParams {
   float scale_log2;         // scale * log2(e)
   int causal_diag;
   unsigned long long wait_limit_ns;
+  int expire_site;          // wait site that gives up at once (0: none; bsa_debug_expire_wait)
 };
 
 // Wait-site ids recorded in the status word's low bits.

@@ -149,6 +149,7 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
+  p.expire_site = lut->expire_site;
   cudaError_t e;
   if (block == 128 && d == 128)
     e = bsa::launch_fwd_b128_d128(p, tq, tk, tv, grid, st);

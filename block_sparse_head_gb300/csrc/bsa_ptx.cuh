@@ -72,6 +72,7 @@ struct WaitCtl {
   volatile int* abort_flag;  // shared memory
   int* status;               // global memory
   uint64_t limit_ns;
+  int expire_site;           // a wait at this site gives up at once (0: none; a test knob)
 };
 
 constexpr int kStatusTimeout = 0x10000;
@@ -95,8 +96,16 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // The common case (the phase completes within a few microseconds) stays inline and never
 // reads the global timer: a handoff through the timed path costs about twice the round
 // trip of a plain spin.  Only a wait that outlasts the spin enters the timed path.
+// Records that the wait at `site` gave up, as a wait that ran out does.
+static __device__ __noinline__ bool mbar_expire(const WaitCtl& ctl, int site) {
+  atomicCAS(ctl.status, 0, kStatusTimeout | site);
+  *ctl.abort_flag = 1;
+  return false;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
                                           int site) {
+  if (site == ctl.expire_site) return mbar_expire(ctl, site);
   if (mbar_test_wait(bar, parity)) return true;
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)

@@ -171,8 +171,11 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
  * call calls no cudaMalloc, cudaFree or other allocating routine.
  *
  *   Arguments q ... stream: as bsa_forward (`lut` need not be uploaded).
- *   sync_status  0: asynchronous, device timeouts are not reported.  Nonzero: the
- *                call synchronizes `stream` after the kernel and returns
+ *   sync_status  0: asynchronous.  A bounded wait that gives up in the kernel is then
+ *                reported to no one (the status word lives in the shared array, not in
+ *                the LUT, so bsa_device_status cannot see it, and the next call clears
+ *                it), and the outputs of that call are undefined.  Nonzero: the call
+ *                synchronizes `stream` after the kernel and returns
  *                BSA_ERR_DEVICE_TIMEOUT if a bounded wait in the kernel gave up.
  *
  * Limit: 4 + 4*n_items + 1024 + nnz int32 words (each part rounded up to 4 words) must
@@ -220,6 +223,22 @@ int bsa_set_schedule(bsa_lut* lut, int policy);
  * and the kernel returns instead of hanging.
  */
 int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns);
+
+/*
+ * bsa_debug_expire_wait -- test knob for the device-side failure path.  Kernels
+ * queued after this call treat every wait at wait site `site` as a wait that ran
+ * out: the waiting role records BSA_ERR_DEVICE_TIMEOUT with that site id in the
+ * status word, raises its CTA's abort flag, and every role of the CTA leaves its
+ * loop, waits for its own copies and MMAs in flight, frees TMEM and returns -- the
+ * same path a real timeout takes, without waiting for one.  The outputs of such a
+ * forward are undefined; bsa_device_status reports it.  site 0 turns the knob off.
+ * Site ids (low 16 bits of the status word): 1 producer, K slot free; 2 producer, V
+ * slot free; 6 MMA issuers, K or V landed; 7 PV issuer, P written; 8 S issuer, S
+ * buffer free; 9 softmax, S computed; 11 softmax, O free for a rescale; 12 softmax,
+ * the item's last PV done.  Errors: BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (site outside
+ * [0, 65535]).
+ */
+int bsa_debug_expire_wait(bsa_lut* lut, int site);
 
 /*
  * bsa_wait_selftest -- launch a one-CTA kernel that waits on a shared-memory

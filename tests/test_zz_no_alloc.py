@@ -5,8 +5,9 @@ deadlock, a memory manager that owns the device heap, a process whose footprint 
 not grow after start-up).  This entry point keeps the LUT's device copy and its status
 word in a fixed array inside the library instead of allocating them.  The test calls
 it through the C ABI twice in a row, with a LUT that was never uploaded, and checks
-each result against the regular bsa_forward within the parity tolerances used by the
-other GPU tests.  It lives in its own file, named to be collected last.
+each result against the regular bsa_forward and against the fp64 oracle, within the
+parity tolerances used by the other GPU tests.  It lives in its own file, named to be
+collected last.
 """
 
 import ctypes
@@ -16,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import block_sparse_head_gb300 as bsa
 from block_sparse_head_gb300 import workloads as wls
 
@@ -34,8 +36,9 @@ def _noalloc(lib, q, k, v, lut, out, lse, scale, block, causal, stream):
 
 
 def _close(o, lse, ro, rl):
-    o, ro = o.float().cpu().numpy(), ro.float().cpu().numpy()
-    lse, rl = lse.cpu().numpy(), rl.cpu().numpy()
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    if isinstance(ro, torch.Tensor):
+        ro, rl = ro.float().cpu().numpy(), rl.cpu().numpy()
     fin = np.isfinite(rl)
     assert np.array_equal(fin, np.isfinite(lse))
     d = np.abs(o - ro)
@@ -70,6 +73,8 @@ def test_noalloc_matches_forward_two_calls(cuda_lib, name, B, block, d, causal, 
     ref_lut = bsa.build_lut(lay, B)  # uploaded: the regular entry point
     ro, rl = bsa.forward(qd, kd, vd, ref_lut, scale, block, causal)
     assert ref_lut.device_status()[0] == 0
+    oo, ol = oracle.forward(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                            np.asarray(lay), scale, block, causal)
     lut = bsa.build_lut(lay, B, upload=False)  # host-only LUT
     stream = torch.cuda.current_stream()
     for _ in range(2):
@@ -78,6 +83,7 @@ def test_noalloc_matches_forward_two_calls(cuda_lib, name, B, block, d, causal, 
         assert _noalloc(lib, qd, kd, vd, lut, out, lse, scale, block, causal, stream) == 0
         torch.cuda.synchronize()
         _close(out, lse, ro, rl)
+        _close(out, lse, oo, ol)
 
 
 def test_noalloc_rejects_oversized_lut(cuda_lib):
