@@ -10,8 +10,11 @@ batch entry) over the whole job, timed with CUDA events on the launching stream.
 Under torchrun every rank runs its own replica of the workload (weak scaling) and the
 slowest rank's time counts.
 
+After the headline the forward is timed alone, by the same method, on the other
+workloads of the 55% target (3 and 4 by default), reported under ``per_workload``.
+
 ``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the same
-workload (query blocks taken in work-list order), on this host's cores.
+workload (query blocks drawn across the work list), one process per host core.
 """
 
 from __future__ import annotations
@@ -126,64 +129,113 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
+_OP = {}  # oracle worker state
+_BLAS_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 
-def _oracle_sample_worker(index: int, budget_s: float, steps: int, warmup: int,
-                          per_step_items: int) -> dict:
-    """Runs in a fresh interpreter: times the oracle on query blocks of the workload."""
+
+def _op_init(tmp, shape, lay, scale, block, causal):
     import numpy as np
 
+    for name in ("q", "k", "v"):
+        _OP[name] = np.memmap(os.path.join(tmp, name), np.float32, "r", shape=shape)
+    _OP["lay"], _OP["par"] = lay, (scale, block, causal)
+
+
+def _op_task(items) -> int:
+    """Oracle over a list of work items (b, h, i, nnz); returns their FLOPs."""
     import oracle
-    from block_sparse_head_gb300 import workloads as wls
 
-    wl = wls.WORKLOADS[index]
-    lay = wls.layout_for(wl).numpy()
-    row_ptr, col_idx, items = oracle.oracle_lut(lay, wl.B)
-    # bf16 -> fp32 is exact; the oracle gathers each item's rows and computes in fp64.
-    q, k, v = (t.float().numpy() for t in wls.qkv(wl))
-    t_load = time.time()
-    step_times, step_flops = [], []
-    pos = 0
-    total_steps = warmup + steps
-    t_begin = time.time()
-    for s in range(total_steps):
+    scale, block, causal = _OP["par"]
+    flops = 0
+    for b, h, i, nnz in items:
+        # mapped fp32 views; the oracle gathers the rows it needs and computes in fp64
+        q, k, v = (_OP[n][b, h] for n in ("q", "k", "v"))
+        oracle.query_block(q, k, v, _OP["lay"][h], scale, block, causal, i)
+        flops += 4 * block * block * q.shape[1] * nnz
+    return flops
+
+
+class OraclePool:
+    """The fp64 oracle, as it stands, over a pool of processes (one per host core).
+
+    The inputs are written once to memory-mapped files that the workers map read only;
+    work items are sampled across the whole work list (a seeded permutation), so the
+    sample mixes long and short rows as the workload does."""
+
+    def __init__(self, wl, q, k, v, lay, procs: int):
+        import multiprocessing as mp
+        import tempfile
+
+        import numpy as np
+        import torch
+
+        import oracle
+
+        self.tmp = tempfile.TemporaryDirectory(prefix="bsa_oracle_")
+        for name, t in (("q", q), ("k", k), ("v", v)):  # bf16 -> fp32 is exact
+            for b in range(t.shape[0]):
+                with open(os.path.join(self.tmp.name, name), "ab") as f:
+                    t[b].float().numpy().tofile(f)
+        lay = np.ascontiguousarray(np.asarray(lay, dtype=np.int64))
+        _, _, items = oracle.oracle_lut(lay, wl.B)
+        perm = np.random.default_rng(0).permutation(len(items))
+        self.items = [tuple(int(x) for x in items[t]) for t in perm]
+        self.pos = 0
+        self.procs = procs
+        # One BLAS thread per worker: the variables must be set before a worker first
+        # imports numpy (unpickling its arguments does), so they go in through the
+        # environment the workers inherit.
+        saved = {var: os.environ.get(var) for var in _BLAS_VARS}
+        os.environ.update({var: "1" for var in _BLAS_VARS})
+        try:
+            self.pool = mp.get_context("spawn").Pool(
+                procs, initializer=_op_init,
+                initargs=(self.tmp.name, tuple(q.shape), lay, wl.scale, wl.block, wl.causal_diag))
+        finally:
+            for var, val in saved.items():
+                if val is None:
+                    os.environ.pop(var, None)
+                else:
+                    os.environ[var] = val
+        self.pool.map(_op_task, [[]] * procs)  # start every worker before timing
+
+    def take(self, n: int) -> list:
+        out = [self.items[(self.pos + j) % len(self.items)] for j in range(n)]
+        self.pos += n
+        return out
+
+    def run(self, n_items: int, per_task: int = 2):
+        """Runs the next n_items sampled items; returns (FLOPs, seconds)."""
+        items = self.take(n_items)
+        tasks = [items[j:j + per_task] for j in range(0, len(items), per_task)]
         t0 = time.perf_counter()
-        flops = 0
-        for _ in range(per_step_items):
-            b, h, i, nnz = (int(x) for x in items[pos % len(items)])
-            pos += 1
-            oracle.query_block(q[b, h], k[b, h], v[b, h], lay[h], wl.scale, wl.block,
-                               wl.causal_diag, i)
-            flops += 4 * wl.block * wl.block * wl.d * nnz
-        dt = time.perf_counter() - t0
-        if s >= warmup:
-            step_times.append(dt)
-            step_flops.append(flops)
-        if budget_s and time.time() - t_begin > budget_s and s >= warmup:
-            break
-    tot_t = sum(step_times)
-    return {"tflops": sum(step_flops) / tot_t / 1e12 if tot_t > 0 else 0.0,
-            "steps_timed": len(step_times), "items_per_step": per_step_items,
-            "seconds": tot_t, "ms_per_step": 1e3 * tot_t / max(1, len(step_times)),
-            "setup_s": t_load - t_begin}
+        flops = sum(self.pool.map(_op_task, tasks, chunksize=1))
+        return flops, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.tmp.cleanup()
 
 
-def run_oracle_subprocess(index: int, budget_s: float, steps: int, warmup: int,
-                          per_step_items: int) -> dict:
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    env = dict(os.environ)
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[var] = str(cores)
-    env["CUDA_VISIBLE_DEVICES"] = ""
-    code = (f"import json,sys; sys.path.insert(0, {ROOT!r}); import bench; "
-            f"print(json.dumps(bench._oracle_sample_worker({index}, {budget_s}, {steps}, "
-            f"{warmup}, {per_step_items})))")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       cwd=ROOT)
-    if r.returncode != 0:
-        raise RuntimeError(f"oracle timing failed:\n{r.stderr[-2000:]}")
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    res["cores"] = cores
-    return res
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline(wl, q, k, v, lay, budget_s: float) -> dict:
+    """Oracle throughput on the host cores: rounds of 2 items per process until
+    `budget_s` seconds of timed work."""
+    procs = host_cores()
+    op = OraclePool(wl, q, k, v, lay, procs)
+    try:
+        flops = secs = 0.0
+        n = 0
+        while secs < budget_s:
+            f, t = op.run(2 * procs)
+            flops, secs, n = flops + f, secs + t, n + 2 * procs
+    finally:
+        op.close()
+    return {"tflops": flops / secs / 1e12, "items": n, "seconds": secs, "cores": procs}
 
 
 # ------------------------------------------------------------------- GPU arm
@@ -213,11 +265,94 @@ def job_tflops(world: int, flops_per_step: int, steps: int, ms: float) -> float:
     return world * flops_per_step * steps / (ms * 1e-3) / 1e12
 
 
+def l2_note_for(wl) -> str:
+    """How the timed region keeps the L2 from serving the inputs of the previous launch."""
+    if 3 * wl.B * wl.H * wl.L * wl.d * 2 < 2 * L2_BYTES:
+        return "L2 flushed between steps (256 MiB write, outside the events)"
+    return "inputs larger than L2"
+
+
 def workload_config(wl, l2_note: str, world: int) -> dict:
     return {"workload": f"{wl.name} (workload {wl.index})", "batch": wl.B, "heads": wl.H,
             "seq_len": wl.L, "block": wl.block, "head_dim": wl.d,
             "causal_diag": bool(wl.causal_diag), "layout": wl.name, "l2": l2_note,
             "parallelism": "replicas" if world > 1 else "single-gpu"}
+
+
+def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds: float,
+                max_steps: int, gpu: int) -> dict:
+    """Device time of the forward alone on workload `index` (no e2e leg): CUDA events
+    around each launch on the launching stream, the L2 flushed between launches when the
+    inputs would fit in it, clocks sampled during the timed region, which lasts at least
+    `min_seconds` (and at least `min_steps` launches)."""
+    import torch
+
+    import block_sparse_head_gb300 as bsa
+    from block_sparse_head_gb300 import workloads as wls
+
+    wl = wls.WORKLOADS[index]
+    lay = wls.layout_for(wl)
+    flops_step = 4 * wl.block * wl.block * wl.d * int(lay.sum()) * wl.B
+    q, k, v = wls.qkv(wl)
+    lut = bsa.build_lut(lay, wl.B, order)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    del q, k, v
+    out = torch.empty_like(qd)
+    lse = torch.empty(wl.B, wl.H, wl.L, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    flush = None
+    l2_note = "inputs larger than L2"
+    if 3 * qd.numel() * 2 < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+        l2_note = "L2 flushed between steps (256 MiB write, outside the events)"
+
+    def step():
+        bsa.forward(qd, kd, vd, lut, wl.scale, wl.block, wl.causal_diag, out=out, lse=lse,
+                    stream=stream)
+
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(5):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = e0.elapsed_time(e1) / 5
+    st, word = lut.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({word:#x}) during warm-up of {wl.name}")
+    n = int(min(max_steps, max(min_steps, math.ceil(min_seconds * 1e3 / max(est_ms, 1e-3)))))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu)
+    time.sleep(0.3)
+    for s in range(n):
+        if flush is not None:
+            flush.fill_(s)
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    st, word = lut.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({word:#x}) in the timed region of {wl.name}")
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(per_ms)
+    peaks = measured_peaks()
+    peak_kind = "bf16_burst" if total_ms < 3000 else "bf16_sustained"
+    achieved = flops_step / (statistics.mean(per_ms) * 1e-3) / 1e12
+    return {"config": workload_config(wl, l2_note, 1), "steps": n,
+            "ms_per_step": round(total_ms / n, 5), "value": round(achieved, 2), "unit": "TFLOPS",
+            "pct_of_peak": round(100 * achieved / peaks[peak_kind], 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks[peak_kind], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks[peak_kind], 4),
+                         "peak_source": f"{peaks['source']} {peak_kind} (MEASURED_PEAKS.json)",
+                         "traffic": recorded_traffic(wl.name), "flops_per_launch": flops_step},
+            "gpu_launches": n, "clocks": clk}
 
 
 def gpu_arm(args) -> None:
@@ -379,14 +514,28 @@ def gpu_arm(args) -> None:
         "wall_s_timed_region": round(t_wall, 3),
         "order": args.order,
     }
-    if not args.no_cpu_baseline and world >= 1:
-        cb = run_oracle_subprocess(wl.index, args.cpu_budget, 10 ** 6, 1, args.cpu_items)
+    extra = [int(x) for x in args.extra_workloads.split(",") if x.strip()] if world == 1 else []
+    if extra:
+        # The forward timed alone on the other target workloads, after the headline, in
+        # the same process and by the same method.
+        del qd, kd, vd, out, lse, slots
+        torch.cuda.empty_cache()
+        line["per_workload"] = {}
+        for index in extra:
+            if index == wl.index:
+                continue
+            r = time_kernel(index, args.order, max(3, args.warmup), args.steps, args.min_seconds,
+                            20000, local)
+            line["per_workload"][wls.WORKLOADS[index].name] = r
+            torch.cuda.empty_cache()
+    if not args.no_cpu_baseline and world == 1:
+        cb = cpu_baseline(wl, q, k, v, lay, args.cpu_budget)
         line["cpu_baseline"] = {
             "value": round(cb["tflops"], 6), "unit": "TFLOPS", "cores": cb["cores"],
             "kind": "oracle",
-            "sample": (f"{cb['steps_timed'] * cb['items_per_step']} query blocks of the workload "
-                       f"in work-list order (longest rows first), {cb['seconds']:.1f} s of fp64 "
-                       "numpy oracle on the host cores")}
+            "sample": (f"{cb['items']} query blocks drawn across the whole work list (seeded "
+                       f"permutation), {cb['seconds']:.1f} s of the fp64 numpy oracle, one "
+                       f"process per host core ({cb['cores']} processes)")}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -399,27 +548,42 @@ def reference_arm(args) -> None:
     from block_sparse_head_gb300 import workloads as wls
 
     wl = wls.WORKLOADS[args.workload]
-    res = run_oracle_subprocess(wl.index, 0.0, args.steps, args.warmup, args.ref_items)
+    lay = wls.layout_for(wl)
+    q, k, v = wls.qkv(wl)
+    procs = host_cores()
+    op = OraclePool(wl, q, k, v, lay, procs)
+    per_step = args.ref_items * procs
+    try:
+        for _ in range(args.warmup):
+            op.run(per_step)
+        flops = secs = 0.0
+        for _ in range(args.steps):
+            f, t = op.run(per_step)
+            flops, secs = flops + f, secs + t
+    finally:
+        op.close()
+    value = flops / secs / 1e12
     line = {
         "metric": METRIC,
-        "value": round(res["tflops"], 6),
+        "value": round(value, 6),
         "unit": "TFLOPS",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(res["ms_per_step"], 3),
+        "ms_per_step": round(1e3 * secs / args.steps, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16; layouts generated from seeds)",
-        "config": workload_config(wl, "host CPU (no GPU)", 1),
+        "config": workload_config(wl, l2_note_for(wl), 1),
         "impl": "reference",
-        "cpu_baseline": {"value": round(res["tflops"], 6), "unit": "TFLOPS", "cores": res["cores"],
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": procs,
                          "kind": "oracle",
-                         "sample": (f"each step = {res['items_per_step']} query blocks of the "
-                                    "workload in work-list order, fp64 numpy oracle")},
-        "e2e": {"value": round(res["tflops"], 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                         "sample": (f"each step = {per_step} query blocks drawn across the "
+                                    "whole work list (seeded permutation), fp64 numpy oracle, "
+                                    f"one process per host core ({procs} processes)")},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -435,8 +599,12 @@ def main() -> None:
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
-    ap.add_argument("--cpu-items", type=int, default=8, help="query blocks per oracle step")
-    ap.add_argument("--ref-items", type=int, default=4, help="query blocks per reference step")
+    ap.add_argument("--ref-items", type=int, default=2,
+                    help="query blocks per host core in each reference step")
+    ap.add_argument("--extra-workloads", default="3,4",
+                    help="other workloads timed (kernel only) after the headline, comma list")
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="shortest timed region of each extra workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
