@@ -1,4 +1,4 @@
-"""fp64 CPU oracle (test infrastructure only; see ``bsa_oracle``)."""
+"""fp64 CPU oracle (test infrastructure only; see ``bsa_oracle`` and ``bsa_oracle_ext``)."""
 
 from .bsa_oracle import (  # noqa: F401
     ORDER_GLOBAL,
@@ -13,3 +13,4 @@ from .bsa_oracle import (  # noqa: F401
     oracle_lut,
     query_block,
 )
+from .bsa_oracle_ext import element_mask, forward_ext, n_blocks  # noqa: F401,E402

@@ -48,15 +48,18 @@ def _case(block, d, growing=False):
     return q, k, v, lay, scale
 
 
-def _check_oracle(q, k, v, lay, scale, block, o, lse):
+def _check_oracle(q, k, v, lay, scale, block, o, lse, rel=0.0):
+    """Parity bars; `rel` adds a bound proportional to |O| for inputs whose scores are
+    so large that attention is nearly one-hot and |O| reaches the |v| extremes, where
+    the bf16 rounding of O alone is up to 2^-8 |O|."""
     ro, rl = oracle.forward(q.double().numpy(), k.double().numpy(), v.double().numpy(),
                             lay.numpy(), scale, block, True)
     o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
     fin = np.isfinite(rl)
     assert np.array_equal(fin, np.isfinite(lse))
     dd = np.abs(o - ro)
-    assert dd.max() <= TOL_MAX and dd.mean() <= TOL_MEAN
-    assert np.abs(lse[fin] - rl[fin]).max() <= TOL_LSE
+    assert np.all(dd <= TOL_MAX + rel * np.abs(ro)) and dd.mean() <= TOL_MEAN
+    assert np.abs(lse[fin] - rl[fin]).max() <= TOL_LSE * max(1.0, rel * np.abs(rl[fin]).max())
 
 
 @pytest.mark.parametrize("block,d", [(128, 128), (64, 128)])
@@ -89,7 +92,7 @@ def test_expired_rescale_wait():
     o0, l0 = bsa.forward(qd, kd, vd, lut, scale, block, True)
     assert lut.device_status()[0] == 0
     o0, l0 = o0.clone(), l0.clone()
-    _check_oracle(q, k, v, lay, scale, block, o0, l0)
+    _check_oracle(q, k, v, lay, scale, block, o0, l0, rel=2.0 ** -7)
     lut.debug_expire_wait(11)
     bsa.forward(qd, kd, vd, lut, scale, block, True)
     st, word = lut.device_status()
