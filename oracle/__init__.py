@@ -4,12 +4,14 @@ from .bsa_oracle import (  # noqa: F401
     ORDER_GLOBAL,
     ORDER_GROUPED,
     active_keys,
+    backward,
     block_flops,
     check_layout,
     expand_mask,
     forward,
     forward_dense,
     masked_attention,
+    oracle_csc,
     oracle_lut,
     query_block,
 )

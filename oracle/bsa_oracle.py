@@ -34,6 +34,10 @@ Sources (page title, then section / equation):
   * "Block Sparse Attention Techniques", section 3.2 "Optimizing Memory Usage with
     Block Sparsity", "Implementation with Sparse Matrix Formats": the active blocks
     are kept in compressed sparse row (CSR) form -> ``oracle_lut``.
+  * "Block Sparse Attention Techniques", section 2, "Gradient Propagation in Block
+    Sparse Attention": gradients flow only through the active blocks -> ``backward``,
+    the gradient of the masked softmax attention above (masked entries have P = 0, so
+    they pass no gradient), written out with the standard softmax Jacobian.
 
 Readings where the pages are silent (each also listed in the design notes):
   * layout values must be exactly 0 or 1;
@@ -260,3 +264,61 @@ def block_flops(layout, batch: int, block: int, d: int) -> int:
     """
     lay = check_layout(layout)
     return int(4 * block * block * d * int(lay.sum()) * batch)
+
+
+# ------------------------------------------------------------------------- backward
+
+
+def backward(q, k, v, do, layout, scale: float, block: int, causal_diag: bool):
+    """Gradients (dq, dk, dv) of sum(O * do) for the forward above, in fp64.
+
+    Per (batch, head), with P the masked softmax of the scaled scores (rows with no
+    active key are all zero):
+        dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(P * dP)),
+        dQ = scale * dS K,   dK = scale * dS^T Q.
+    Masked entries have P = 0 and so pass no gradient ("Block Sparse Attention
+    Techniques", section 2, gradient propagation through active blocks only).
+    q, k, v, do: [B, H, L, d].  Returns (dq, dk, dv), each [B, H, L, d] fp64.
+    """
+    lay = check_layout(layout)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, L, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for h in range(H):
+        mask = expand_mask(lay[h], block, L, causal_diag)
+        for b in range(B):
+            s = np.where(mask, scale * (q[b, h] @ k[b, h].T), -np.inf)
+            p = np.zeros((L, L))
+            for r in range(L):
+                if mask[r].any():
+                    e = np.exp(s[r] - s[r].max())
+                    p[r] = e / e.sum()
+            dv[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
+def oracle_csc(layout, batch: int):
+    """Column view of the layout for the key-side gradients: for each (h, j) the active
+    query blocks i ascending (col_ptr [H*nb+1], row_idx [nnz]) and one item
+    {b, h, j, count} per (batch, head, key block), sorted by (-count, b, h, j)."""
+    lay = check_layout(layout)
+    H, nb, _ = lay.shape
+    col_ptr = [0]
+    row_idx: list[int] = []
+    for h in range(H):
+        for j in range(nb):
+            rows = [int(i) for i in np.nonzero(lay[h, :, j] == 1)[0]]
+            row_idx.extend(rows)
+            col_ptr.append(col_ptr[-1] + len(rows))
+    items = [(b, h, j, col_ptr[h * nb + j + 1] - col_ptr[h * nb + j])
+             for b in range(batch) for h in range(H) for j in range(nb)]
+    items.sort(key=lambda it: (-it[3], it[0], it[1], it[2]))
+    return (np.asarray(col_ptr, np.int32), np.asarray(row_idx, np.int32),
+            np.asarray(items, np.int32).reshape(-1, 4))
