@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     Lut,
     build_lut,
     forward,
+    forward_ext,
     library_path,
     load_library,
 )

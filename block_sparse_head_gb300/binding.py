@@ -30,7 +30,15 @@ EXPORTED = (
     "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
     "bsa_wait_selftest",
     "bsa_status_string", "bsa_version", "bsa_forward_noalloc", "bsa_debug_expire_wait",
+    "bsa_build_lut_rect", "bsa_lut_kv_blocks", "bsa_forward_ext",
 )
+
+
+class ExtArgs(ctypes.Structure):
+    """bsa_ext_args of include/bsa.h."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("softcap", ctypes.c_float), ("sinks", ctypes.c_void_p),
+                ("q_segment_ids", ctypes.c_void_p), ("kv_segment_ids", ctypes.c_void_p)]
 
 _lib = None
 _lock = threading.Lock()
@@ -64,6 +72,13 @@ def load_library():
         vp = ctypes.c_void_p
         lib.bsa_build_lut.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(vp)]
+        lib.bsa_build_lut_rect.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
+        lib.bsa_lut_kv_blocks.argtypes = [vp, ip]
+        lib.bsa_forward_ext.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(ExtArgs), vp]
         lib.bsa_lut_info.argtypes = [vp, ip, ip, ip, ip, ip]
         lib.bsa_lut_export.argtypes = [vp, vp, vp, vp]
         lib.bsa_lut_schedule.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
@@ -89,7 +104,8 @@ def load_library():
         for name in ("bsa_build_lut", "bsa_lut_info", "bsa_lut_export", "bsa_lut_schedule",
                      "bsa_lut_upload",
                      "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
-                     "bsa_wait_selftest", "bsa_debug_expire_wait"):
+                     "bsa_wait_selftest", "bsa_debug_expire_wait", "bsa_build_lut_rect",
+                     "bsa_lut_kv_blocks", "bsa_forward_ext"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -112,17 +128,23 @@ class Lut:
     def __init__(self, layout, batch: int, order="global"):
         lib = load_library()
         lay = layout.detach().cpu().numpy() if isinstance(layout, torch.Tensor) else np.asarray(layout)
-        if lay.ndim != 3 or lay.shape[1] != lay.shape[2]:
-            raise ValueError(f"layout must be [H, nb, nb], got {lay.shape}")
+        if lay.ndim != 3:
+            raise ValueError(f"layout must be [H, nb, nbk], got {lay.shape}")
         lay = np.ascontiguousarray(lay.astype(np.int32, copy=False))
         self._lib = lib
         self.handle = ctypes.c_void_p()
-        _check(lib.bsa_build_lut(lay.ctypes.data, lay.shape[0], lay.shape[1], int(batch),
-                                 _ORDERS[order], ctypes.byref(self.handle)), "bsa_build_lut")
-        H, nb, b, nnz, n = (ctypes.c_int() for _ in range(5))
+        if lay.shape[1] == lay.shape[2]:
+            _check(lib.bsa_build_lut(lay.ctypes.data, lay.shape[0], lay.shape[1], int(batch),
+                                     _ORDERS[order], ctypes.byref(self.handle)), "bsa_build_lut")
+        else:
+            _check(lib.bsa_build_lut_rect(lay.ctypes.data, lay.shape[0], lay.shape[1],
+                                          lay.shape[2], int(batch), _ORDERS[order],
+                                          ctypes.byref(self.handle)), "bsa_build_lut_rect")
+        H, nb, b, nnz, n, nbk = (ctypes.c_int() for _ in range(6))
         _check(lib.bsa_lut_info(self.handle, *(ctypes.byref(x) for x in (H, nb, b, nnz, n))),
                "bsa_lut_info")
-        self.H, self.nb, self.batch = H.value, nb.value, b.value
+        _check(lib.bsa_lut_kv_blocks(self.handle, ctypes.byref(nbk)), "bsa_lut_kv_blocks")
+        self.H, self.nb, self.batch, self.nbk = H.value, nb.value, b.value, nbk.value
         self.nnz_total, self.n_items = nnz.value, n.value
         self.device = None
 
@@ -214,6 +236,51 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: 
     _check(lib.bsa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), lut.handle, out.data_ptr(),
                            lse.data_ptr(), B, H, L, d, float(scale), int(block), int(bool(causal_diag)),
                            _stream_handle(stream)), "bsa_forward")
+    return out, lse
+
+
+def forward_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: float,
+                q_block: int, kv_block: int, causal_diag: bool, window=None, softcap: float = 0.0,
+                sinks: torch.Tensor | None = None, q_segment_ids: torch.Tensor | None = None,
+                kv_segment_ids: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, stream=None):
+    """Extended forward (bsa_forward_ext): q [B,H,Lq,d], k/v [B,H,Lk,d] bf16; ``window``
+    an int (both sides) or a (left, right) pair (None or negative: no bound); ``sinks``
+    fp32 [H]; segment ids int32 [B,Lq] / [B,Lk].  Returns (out [B,H,Lq,d], lse [B,H,Lq])."""
+    lib = load_library()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    _check_qkv(q, "q", (B, H, Lq, d))
+    _check_qkv(k, "k", (B, H, Lk, d))
+    _check_qkv(v, "v", (B, H, Lk, d))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Lq, device=q.device, dtype=torch.float32)
+    _check_qkv(out, "out", (B, H, Lq, d))
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Lq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Lq] tensor")
+    if window is None:
+        wl = wr = -1
+    elif isinstance(window, int):
+        wl = wr = window
+    else:
+        wl, wr = (-1 if w is None else int(w) for w in window)
+
+    def dev_arr(t, dtype, shape, name):
+        if t is None:
+            return None
+        if not t.is_cuda or t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor of shape {shape}")
+        return t.data_ptr()
+
+    x = ExtArgs(wl, wr, float(softcap), dev_arr(sinks, torch.float32, (H,), "sinks"),
+                dev_arr(q_segment_ids, torch.int32, (B, Lq), "q_segment_ids"),
+                dev_arr(kv_segment_ids, torch.int32, (B, Lk), "kv_segment_ids"))
+    _check(lib.bsa_forward_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), lut.handle,
+                               out.data_ptr(), lse.data_ptr(), B, H, Lq, Lk, d, float(scale),
+                               int(q_block), int(kv_block), int(bool(causal_diag)),
+                               ctypes.byref(x), _stream_handle(stream)), "bsa_forward_ext")
     return out, lse
 
 

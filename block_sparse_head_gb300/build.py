@@ -22,12 +22,9 @@ LIB = os.path.join(PKG, "libbsa.so")
 SOURCES = [
     "bsa_host.cpp",
     "bsa_selftest.cu",
-    "bsa_fwd_b128_d128.cu",
-    "bsa_fwd_b128_d64.cu",
-    "bsa_fwd_b64_d128.cu",
-    "bsa_fwd_b64_d64.cu",
     "bsa_noalloc.cu",
-]
+] + [f"bsa_fwd_q{qb}_k{kb}_d{d}.cu" for qb, kb in ((64, 64), (128, 128), (64, 128), (128, 64))
+     for d in (64, 128)]
 HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_fwd_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -8,8 +8,10 @@
 // Techniques" (sections 3.2 and 4) and the DeepSpeed sparse-attention utils page.
 // Scores outside the active blocks are never formed: their exp() would be 0.
 //
-// Keys are consumed in steps of 128 rows: one block when b = 128, the next two active
-// blocks of the row when b = 64 (the last step of a row with an odd count holds one).
+// Query blocks have QB rows and key blocks KB keys (64 or 128 each; equal in the plain
+// kernels).  Keys are consumed in steps of 128: one block when KB = 128, the next two
+// active blocks of the row when KB = 64 (the last step of a row with an odd count holds
+// one).
 // A CTA walks its own range of the work list, regrouped per CTA on the host (each item to
 // the least-loaded CTA), as one continuous stream of steps g = 0, 1, ...
 //
@@ -42,6 +44,15 @@
 // position) are fetched two items ahead and column indices one step ahead of use, so no
 // role waits on a global load in its steady state.
 //
+// The extended kernels (EXT) add per-element predicates on the same path, following the
+// ejkernel blocksparse_attention arguments: a key past the end of a ragged sequence, a
+// key outside the sliding window (left, right) of its query, a key of another segment
+// (packed sequences), and the diagonal mask in every key block that overlaps the query
+// block's rows, are all masked to -inf; the scores may be soft-capped
+// (cap * tanh(s / cap)); and a per-head sink logit joins the softmax normaliser (the
+// DeepSeek-V4.1 sparse_attn kernel's attn_sink) without a value row.  Rows past the end
+// of a ragged query sequence are computed but not stored.
+//
 // Every barrier wait is bounded (WaitCtl): a wait that runs out records a timeout in
 // the status word, and all roles leave their loops, drain in-flight copies and MMAs,
 // free TMEM and return.
@@ -54,31 +65,31 @@
 
 namespace bsa {
 
-template <int BLK, int D>
+template <int QB, int KB, int D>
 struct FwdCfg {
-  static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
+  static_assert(QB == 64 || QB == 128, "query block must be 64 or 128");
+  static_assert(KB == 64 || KB == 128, "key block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-  static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // softmax warpgroups
+  static constexpr int kNumWG = (QB == 128) ? 2 : 1;  // softmax warpgroups
   static constexpr int kPvWarp = 2 + 4 * kNumWG;       // after the softmax warps
   static constexpr int kThreads = 32 * (kPvWarp + 1);  // producer, S issuer, softmax, PV issuer
   static constexpr int kKR = 128;                 // key rows per step
-  static constexpr int kG = kKR / BLK;            // blocks per step (1 or 2)
+  static constexpr int kG = kKR / KB;             // blocks per step (1 or 2)
   static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
   static constexpr int kNK = 3;                   // K tiles in shared memory
-  static constexpr int kQTileB = BLK * D * 2;     // (bytes of one Q tile, for the budget below)
+  static constexpr int kQTileB = QB * D * 2;      // (bytes of one Q tile, for the budget below)
   static constexpr int kKVTileB = 128 * D * 2;
   // Two Q tiles, so the next item's Q loads while the current item's last S runs; V gets
   // three tiles when they fit beside them, else two (b = 128, d = 128).
   static constexpr int kNV = (2 * kQTileB + 6 * kKVTileB + 1216 <= 232448) ? 3 : 2;  // V tiles
-  static constexpr int kQTile = BLK * D * 2;      // bytes of one Q tile
+  static constexpr int kQTile = QB * D * 2;       // bytes of one Q tile
   static constexpr int kKVTile = kKR * D * 2;     // bytes of one K or V step tile
-  // Q tiles: two when they fit beside the K/V tiles, else one (b = 128, d = 128).
-  static constexpr int kNQ = 2;
-  static constexpr int kQRegion = BLK * 128;      // one 64-column swizzled box of BLK rows
+  static constexpr int kNQ = 2;                   // Q tiles
+  static constexpr int kQRegion = QB * 128;       // one 64-column swizzled box of QB rows
   // A K or V step tile holds its blocks one after another, each as d/64 swizzled
-  // [b][64] column halves (the layout one 3-D TMA copy of a block lands in).
-  static constexpr int kHalfB = BLK * 128;        // one 64-column half of one block
-  static constexpr int kBlkB = BLK * D * 2;       // one block
+  // [KB][64] column halves (the layout one 3-D TMA copy of a block lands in).
+  static constexpr int kHalfB = KB * 128;         // one 64-column half of one block
+  static constexpr int kBlkB = KB * D * 2;        // one block
   static constexpr int kOCol = kNS * 128;         // O after the S buffers
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
@@ -104,9 +115,9 @@ struct FwdCfg {
   // tcgen05.alloc until the first, persistent, CTA finished).
   static constexpr int kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
   // instruction descriptors: S over a full step (N = 128) or a single 64-key block
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(BLK, kKR, false, false);
-  static constexpr uint32_t kIdescS1 = idesc_bf16_f32(BLK, BLK, false, false);
-  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BLK, D, false, true);
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(QB, kKR, false, false);
+  static constexpr uint32_t kIdescS1 = idesc_bf16_f32(QB, KB, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(QB, D, false, true);
 };
 
 // Bounded wait that ignores the abort flag and never records a status: used only
@@ -130,11 +141,11 @@ __device__ __forceinline__ int step_blocks(int nnz, int s) {
 }
 
 // The CTA's share of the work list: items[cta_start[c] .. cta_start[c+1]) for CTA c, as
-// device records {q_blk, kv_blk, rs, nnz | (dpos + 1) << 16}: the item's query block
-// among all B*H*nb (its rows start at q_blk * b), the first block of its (batch, head)'s
-// K and V (block j starts at row (kv_blk + j) * b), its row's first col_idx entry, its
-// active block count and the position of block i in its row (-1: none).  w = 0 marks an
-// empty item, w = -1 the end.  Records are fetched two items ahead of use.
+// device records {bh, i, rs, nnz | (dpos + 1) << 16}: the item's (batch, head) pair
+// bh = b * H + h and query block i (its rows start at row bh * Lq + i * QB of Q and O;
+// key block j of the pair at row bh * Lk + j * KB of K and V), its row's first col_idx
+// entry, its active block count and the position of block i in its row (-1: none).
+// w = 0 marks an empty item, w = -1 the end.  Records are fetched two items ahead of use.
 struct ItemStream {
   int t;                 // work-list index of the current item
   int end;               // one past the CTA's last item
@@ -195,11 +206,11 @@ struct StepCursor {
 
 // ----------------------------------------------------------------- producer
 
-template <int BLK, int D>
+template <int QB, int KB, int D>
 __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint32_t sbase, const WaitCtl& ctl) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   constexpr int G = C::kG;
   static_assert(C::kNK == 3, "K slot reuse is tied to the three S buffers");
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
@@ -232,15 +243,15 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
     int qrow = 0, qb = 0;
     if (c.valid()) {
       r0.nblk = c.nblk();
+      const int kv0 = c.is.cur.x * p.Lk;  // first K/V row of the item's (batch, head)
 #pragma unroll
-      for (int g = 0; g < G; ++g) r0.krow[g] = (c.is.cur.y + colv[g]) * BLK;
+      for (int g = 0; g < G; ++g) r0.krow[g] = kv0 + colv[g] * KB;
       first = (c.s == 0);
-      qrow = c.is.cur.x * BLK;
+      qrow = c.is.cur.x * p.Lq + c.is.cur.y * QB;
       qb = c.is.n % C::kNQ;
       if (first && c.is.nx1.w > 0) {
         // Warm L2 with the following item's Q.
-        const int nrow = c.is.nx1.x * BLK;
-#pragma unroll
+        const int nrow = c.is.nx1.x * p.Lq + c.is.nx1.y * QB;
         tma_prefetch_l2_3d(tm_q, 0, nrow, 0);
       }
       c.advance(p);
@@ -259,7 +270,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       if (first) j = max(j, t - (C::kNQ == 1 ? 1 : 2));
       if (j >= 0 && !mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
       const uint32_t fb = bar(C::kBarKF + t % 3);
-      mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * BLK * D * 2);
+      mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * C::kBlkB);
       ++nk;
       // One copy per tile or block, all column halves at once.
       if (first) tma_load_3d(sbase + C::kOffQ + qb * C::kQTile, tm_q, fb, 0, qrow, 0);
@@ -277,7 +288,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       if (gv >= 0 && !mbar_wait(bar(C::kBarPVD + gv % 3), (gv / 3) & 1, ctl, kSiteProdVEmpty))
         break;
       const uint32_t fb = bar(C::kBarVF + g % 3);
-      mbar_arrive_expect_tx(fb, rv.nblk * BLK * D * 2);
+      mbar_arrive_expect_tx(fb, rv.nblk * C::kBlkB);
       ++nv;
       const uint32_t vdst = sbase + C::kOffV + (g % C::kNV) * C::kKVTile;
 #pragma unroll
@@ -299,9 +310,9 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
 
 // Shared-memory descriptors are built once; per MMA only the low word (start address >> 4)
 // moves.  K and Q are K-major, V is MN-major; all three share the high word.
-template <int BLK, int D>
+template <int QB, int KB, int D>
 struct MmaDescs {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   uint32_t hi, k0, v0, q0;
   __device__ __forceinline__ explicit MmaDescs(uint32_t sbase) {
     const uint64_t kdesc0 = sdesc_sw128(sbase + C::kOffK, 16, 1024);
@@ -313,13 +324,13 @@ struct MmaDescs {
 };
 
 // S(t) = Q K(t)^T into S[t % 3].
-template <int BLK, int D>
+template <int QB, int KB, int D>
 __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                           const WaitCtl& ctl) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  const MmaDescs<BLK, D> md(sbase);
+  const MmaDescs<QB, KB, D> md(sbase);
   constexpr uint32_t kTileStep = C::kKVTile >> 4;  // descriptor units per K/V tile
   StepCursor<G> c;
   c.init(p);
@@ -334,19 +345,19 @@ __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, ui
     const uint32_t sb = tmem + (t % 3) * 128;
     const uint32_t qlo = md.q0 + qb * (C::kQTile >> 4);
     const uint32_t klo = md.k0 + (t % 3) * kTileStep;
-    // b = 128: one N = 128 MMA per 16 columns of d.  b = 64: one N = 64 MMA per block
+    // KB = 128: one N = 128 MMA per 16 columns of d.  KB = 64: one N = 64 MMA per block
     // (the blocks' rows are not contiguous), into S columns [64g, 64g + 64).
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t qa = qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4);
       const uint32_t kb = klo + (((kk >> 2) * C::kHalfB + (kk & 3) * 32) >> 4);
-      if (BLK == 128) {
+      if (KB == 128) {
         tc_mma_ss_lh(sb, qa, md.hi, kb, md.hi, C::kIdescS, kk > 0 ? 1u : 0u);
       } else {
 #pragma unroll
         for (int g = 0; g < G; ++g)
           if (g < nblk)
-            tc_mma_ss_lh(sb + g * BLK, qa, md.hi, kb + ((g * C::kBlkB) >> 4), md.hi, C::kIdescS1,
+            tc_mma_ss_lh(sb + g * KB, qa, md.hi, kb + ((g * C::kBlkB) >> 4), md.hi, C::kIdescS1,
                          kk > 0 ? 1u : 0u);
       }
     }
@@ -358,13 +369,13 @@ __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, ui
 }
 
 // O += P(g) V(g), P read from S[g % 3].
-template <int BLK, int D>
+template <int QB, int KB, int D>
 __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                            const WaitCtl& ctl) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  const MmaDescs<BLK, D> md(sbase);
+  const MmaDescs<QB, KB, D> md(sbase);
   constexpr uint32_t kTileStep = C::kKVTile >> 4;
   StepCursor<G> c;
   c.init(p);
@@ -379,13 +390,13 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
     const uint32_t ps = tmem + (g % 3) * 128;
     const uint32_t od = tmem + C::kOCol;
     const uint32_t vlo = md.v0 + (g % C::kNV) * kTileStep;
-    const int ksteps = nblk * BLK / 16;
+    const int ksteps = nblk * KB / 16;
     tc_mma_ts_lh(od, ps, vlo, md.hi, C::kIdescPV, first ? 0u : 1u);
 #pragma unroll
     for (int kk = 1; kk < C::kKR / 16; ++kk)
       if (kk < ksteps)
         tc_mma_ts_lh(od, ps + kk * 8,
-                     vlo + ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4), md.hi,
+                     vlo + ((((kk * 16) / KB) * C::kBlkB + ((kk * 16) % KB) * 128) >> 4), md.hi,
                      C::kIdescPV, 1u);
     tc_commit(bar(C::kBarPVD + g % 3));
   }
@@ -444,37 +455,59 @@ __device__ __forceinline__ void store_o(const FwdParams& p, int qrow, int half,
   if (half == 0) p.lse[qrow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
-template <int BLK, int D>
+// tanh(z) = 1 - 2 / (1 + e^(2z)); e^(2z) from ex2 gives the exact limits +-1 for large
+// |z| (the quotient goes to 0 or 2).
+__device__ __forceinline__ float tanh_via_ex2(float z) {
+  return 1.f - __fdividef(2.f, 1.f + ex2_approx(z * 2.8853900817779268f));
+}
+
+// The final (m, l) of a row and the factor its O accumulator is scaled by.  With a sink
+// logit t (log2 units; -inf when there is none) the normaliser gains the term 2^t:
+// m' = max(m, t), l' = l 2^(m - m') + 2^(t - m'), O / l' scaled by 2^(m - m').
+__device__ __forceinline__ float finish_row(float& m, float& l, float t) {
+  if (t == -INFINITY) return (l > 0.f) ? 1.f / l : 0.f;
+  const float mf = fmaxf(m, t);
+  const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mf);
+  l = l * a + ex2_approx(t - mf);
+  m = mf;
+  return a / l;
+}
+
+template <int QB, int KB, int D, bool EXT>
 __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                             const WaitCtl& ctl) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   constexpr int G = C::kG;
   constexpr int NC = 64;      // score columns per thread
   constexpr int OC = D / 2;   // O columns per thread
   constexpr int NA = 8;       // independent max chains
   constexpr int NS = 4;       // packed sum accumulators
+  constexpr float kLog2e = 1.4426950408889634f;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   const int wg = ((threadIdx.x >> 5) - 2) >> 2;  // softmax group (warps 2-5, 6-9)
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   // Row of the query block held by this lane pair, and the TMEM lane base of the warp.
-  const int row = (BLK == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
-  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (BLK == 128 ? wg * 16 : 0)) << 16);
+  const int row = (QB == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
+  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (QB == 128 ? wg * 16 : 0)) << 16);
   const uint32_t to = tl + C::kOCol;
-  // b = 128: this half holds keys [64*half, 64*half + 64) of the step's block.
-  // b = 64: this half holds block `half` of the step (all of its 64 keys).
-  const int kbase = (BLK == 128) ? 64 * half : 0;
+  // This half holds keys [64*half, 64*half + 64) of the step: half of the block when
+  // KB = 128, block `half` of the step (all of its 64 keys) when KB = 64.
+  const int kbase = (KB == 128) ? 64 * half : 0;
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
   // scale > 0: the row max of the raw scores gives the max of the scaled ones and the
-  // exponent is one FFMA.  Otherwise the scores are scaled first (c = 1 afterwards).
-  const bool pos_scale = p.scale_log2 > 0.f;
+  // exponent is one FFMA.  Otherwise (and always in the extended kernels, which transform
+  // the scores first) the scores are scaled first (c = 1 afterwards).
+  const bool pos_scale = !EXT && p.scale_log2 > 0.f;
   const float cs = pos_scale ? p.scale_log2 : 1.f;
   int g = 0;
   bool ok = true;
   bool have_pending = false;
   int pend_row = 0;
   float pend_m = 0.f, pend_l = 0.f;
+  bool pend_ok = true;            // (EXT) the pending row lies inside the sequence
+  float pend_t = -INFINITY;       // (EXT) the pending row's sink logit, log2 units
   // S(g+1) already complete, as seen by a probe issued during step g (its latency then
   // overlaps the end of step g instead of opening step g+1).
   bool s_next = false;
@@ -496,23 +529,45 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   ItemStream is;
   for (is.init<false>(p); ok && !is.done(); is.next<false>(p)) {
     const int nnz = is.nnz();
-    const int qrow = is.cur.x * BLK + row;  // global query row
+    const int qrow = is.cur.x * p.Lq + is.cur.y * QB + row;  // global query row
+    // (EXT) the row's position in its sequence, batch, head, segment and sink
+    int qpos = 0, qseg = 0;
+    bool row_ok = true;
+    float sink_t = -INFINITY;
+    const int32_t* kvseg = nullptr;
+    if constexpr (EXT) {
+      qpos = is.cur.y * QB + row;
+      row_ok = qpos < p.Lq;
+      const int bi = is.cur.x / p.H;
+      if (p.sinks != nullptr) sink_t = p.sinks[is.cur.x - bi * p.H] * kLog2e;
+      if (p.kv_seg != nullptr) {
+        kvseg = p.kv_seg + static_cast<size_t>(bi) * p.Lk;
+        qseg = row_ok ? p.q_seg[static_cast<size_t>(bi) * p.Lq + qpos] : 0;
+      }
+    }
     if (nnz == 0) {
-      uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
+      if (row_ok) {
+        uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
 #pragma unroll
-      for (int c = 0; c < OC / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-      if (half == 0) p.lse[qrow] = -INFINITY;
+        for (int c = 0; c < OC / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        if (half == 0) p.lse[qrow] = (sink_t == -INFINITY) ? -INFINITY : sink_t / kLog2e;
+      }
       continue;
     }
-    const int dpos = p.causal_diag ? is.dpos() : -1;  // position of block i in the row
+    const int dpos = (!EXT && p.causal_diag) ? is.dpos() : -1;  // position of block i in the row
     const int nsteps = (nnz + G - 1) / G;
     float m_used = -INFINITY;
     float l = 0.f;
     for (int s = 0; s < nsteps; ++s, ++g) {
       const int nblk = step_blocks<G>(nnz, s);
-      const bool valid = (BLK == 128) || (half < nblk);
-      const bool diag = valid && (((BLK == 128) ? s : s * 2 + half) == dpos);
+      const bool valid = (KB == 128) || (half < nblk);
+      const bool diag = !EXT && valid && (((KB == 128) ? s : s * 2 + half) == dpos);
       const uint32_t ts = tl + (g % 3) * 128;
+      // (EXT) key block of this half's keys; the load overlaps the S wait
+      int colh = 0;
+      if constexpr (EXT) {
+        if (valid) colh = p.col_idx[is.cur.z + s * G + (KB == 64 ? half : 0)];
+      }
       if (__all_sync(0xffffffffu, s_next)) {
         tc_fence_after();
       } else {
@@ -532,19 +587,55 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
           x[32 + i] = __uint_as_float(r1[i]);
         }
       }
-      if (!pos_scale) {
+      if constexpr (EXT) {
+        // Scores in log2 units: soft-capped (cap * log2e * tanh(s / cap)) or scaled.
+        if (p.softcap_log2 > 0.f) {
 #pragma unroll
-        for (int c = 0; c < NC; ++c) x[c] *= p.scale_log2;
-      }
-      if (!valid) {
+          for (int c = 0; c < NC; ++c) x[c] = p.softcap_log2 * tanh_via_ex2(x[c] * p.softcap_inv);
+        } else {
 #pragma unroll
-        for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
-      } else if (diag) {
-        // Key kbase + c is masked when it lies after the query row.  Predicated selects:
-        // written as branches, the per-lane bounds made this step twice as slow.
-        const int qin = row - kbase;
+          for (int c = 0; c < NC; ++c) x[c] *= p.scale_log2;
+        }
+        // Keys kpos0 + c allowed for c in [lo, hi]: inside the sequence, the window, and
+        // (in a key block overlapping the query block's rows, with causal_diag) not after
+        // the query.
+        const int kpos0 = colh * KB + kbase;
+        int lo = 0;
+        int hi = min(NC - 1, p.Lk - 1 - kpos0);
+        if (!row_ok || !valid) hi = -1;
+        if (p.window_left >= 0) lo = max(lo, qpos - p.window_left - kpos0);
+        if (p.window_right >= 0) hi = min(hi, qpos + p.window_right - kpos0);
+        if (p.causal_diag) {
+          const int k0 = colh * KB;
+          if (k0 < (is.cur.y + 1) * QB && k0 + KB > is.cur.y * QB) hi = min(hi, qpos - kpos0);
+        }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) x[c] = mask_gt(x[c], c, qin);
+        for (int c = 0; c < NC; ++c) x[c] = mask_outside(x[c], c, lo, hi);
+        if (kvseg != nullptr && hi >= lo) {
+          // Keys of another segment; only keys inside [lo, hi] (so inside the sequence)
+          // are read.
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const bool in = (c >= lo) && (c <= hi);
+            const int sg = in ? __ldg(kvseg + kpos0 + c) : qseg;
+            if (sg != qseg) x[c] = -INFINITY;
+          }
+        }
+      } else {
+        if (!pos_scale) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) x[c] *= p.scale_log2;
+        }
+        if (!valid) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
+        } else if (diag) {
+          // Key kbase + c is masked when it lies after the query row.  Predicated selects:
+          // written as branches, the per-lane bounds made this step twice as slow.
+          const int qin = row - kbase;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) x[c] = mask_gt(x[c], c, qin);
+        }
       }
       // Row max: NA chains of three-input maxima over columns c = a (mod NA), then the
       // other half of the row (lane ^ 16).
@@ -617,12 +708,14 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       if (s == 0 && have_pending) {
         ok = wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone);
         if (!ok) break;
-        read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
+        const float inv = EXT ? finish_row(pend_m, pend_l, pend_t)
+                              : ((pend_l > 0.f) ? 1.f / pend_l : 0.f);
+        read_o<D>(to, inv, opk);
       }
       tmem_st_wait();
       warp_arrive(C::kBarPF + g % 3);
       if (s == 0 && have_pending) {
-        store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
+        if (pend_ok) store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
         have_pending = false;
       }
     }
@@ -630,23 +723,27 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
     pend_row = qrow;
     pend_m = m_used;
     pend_l = l;
+    pend_ok = row_ok;
+    pend_t = sink_t;
     have_pending = true;
   }
   if (ok && have_pending &&
       wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone)) {
     uint32_t opk[D / 4];
-    read_o<D>(to, (pend_l > 0.f) ? 1.f / pend_l : 0.f, opk);
-    store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
+    const float inv = EXT ? finish_row(pend_m, pend_l, pend_t)
+                          : ((pend_l > 0.f) ? 1.f / pend_l : 0.f);
+    read_o<D>(to, inv, opk);
+    if (pend_ok) store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
   }
 }
 
 // ------------------------------------------------------------------- kernel
 
-template <int BLK, int D>
-__global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
+template <int QB, int KB, int D, bool EXT>
+__global__ void __launch_bounds__(FwdCfg<QB, KB, D>::kThreads, 1)
     bsa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -686,13 +783,13 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, p.expire_site};
 
   if (warp == 0) {
-    if (lane == 0) fwd_producer<BLK, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
+    if (lane == 0) fwd_producer<QB, KB, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
   } else if (warp == 1) {
-    if (lane == 0) fwd_mma_s<BLK, D>(p, sbase, tmem, ctl);
+    if (lane == 0) fwd_mma_s<QB, KB, D>(p, sbase, tmem, ctl);
   } else if (warp == C::kPvWarp) {
-    if (lane == 0) fwd_mma_pv<BLK, D>(p, sbase, tmem, ctl);
+    if (lane == 0) fwd_mma_pv<QB, KB, D>(p, sbase, tmem, ctl);
   } else {
-    fwd_softmax<BLK, D>(p, sbase, tmem, ctl);
+    fwd_softmax<QB, KB, D, EXT>(p, sbase, tmem, ctl);
   }
 
   tc_fence_before();
@@ -704,21 +801,21 @@ __global__ void __launch_bounds__(FwdCfg<BLK, D>::kThreads, 1)
   }
 }
 
-template <int BLK, int D>
+template <int QB, int KB, int D, bool EXT>
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
                        const CUtensorMap& v, int grid, cudaStream_t stream) {
-  using C = FwdCfg<BLK, D>;
+  using C = FwdCfg<QB, KB, D>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(bsa_fwd_kernel<BLK, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kLaunchSmem);
+    e = cudaFuncSetAttribute(bsa_fwd_kernel<QB, KB, D, EXT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  bsa_fwd_kernel<BLK, D><<<grid, C::kThreads, C::kLaunchSmem, stream>>>(q, k, v, p);
+  bsa_fwd_kernel<QB, KB, D, EXT><<<grid, C::kThreads, C::kLaunchSmem, stream>>>(q, k, v, p);
   return cudaGetLastError();
 }
 

@@ -135,12 +135,28 @@ void bsa::device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
   for (size_t k = 0; k + 3 < items.size(); k += 4) {
     const int32_t b = items[k], h = items[k + 1], i = items[k + 2], nnz = items[k + 3];
     const int32_t row = h * lut.nb + i;
-    const int32_t kv = (b * lut.H + h) * lut.nb;
-    records[k] = kv + i;
-    records[k + 1] = kv;
+    records[k] = b * lut.H + h;
+    records[k + 1] = i;
     records[k + 2] = lut.row_ptr[static_cast<size_t>(row)];
     records[k + 3] = nnz | ((lut.diag_pos[static_cast<size_t>(row)] + 1) << 16);
   }
+}
+
+cudaError_t bsa::launch_fwd_variant(int q_block, int kv_block, int d, bool ext,
+                                    const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                                    const CUtensorMap& v, int grid, cudaStream_t stream) {
+  const bool d128 = d == 128;
+  if (q_block == 64 && kv_block == 64)
+    return d128 ? launch_fwd_q64_k64_d128(ext, p, q, k, v, grid, stream)
+                : launch_fwd_q64_k64_d64(ext, p, q, k, v, grid, stream);
+  if (q_block == 128 && kv_block == 128)
+    return d128 ? launch_fwd_q128_k128_d128(ext, p, q, k, v, grid, stream)
+                : launch_fwd_q128_k128_d64(ext, p, q, k, v, grid, stream);
+  if (q_block == 64 && kv_block == 128)
+    return d128 ? launch_fwd_q64_k128_d128(ext, p, q, k, v, grid, stream)
+                : launch_fwd_q64_k128_d64(ext, p, q, k, v, grid, stream);
+  return d128 ? launch_fwd_q128_k64_d128(ext, p, q, k, v, grid, stream)
+              : launch_fwd_q128_k64_d64(ext, p, q, k, v, grid, stream);
 }
 
 bool bsa::schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t d, int dev) {
@@ -176,13 +192,18 @@ void free_device(bsa_lut* lut) {
 extern "C" {
 
 int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bsa_lut** out) {
+  return bsa_build_lut_rect(layout, H, nb, nb, batch, order, out);
+}
+
+int bsa_build_lut_rect(const int32_t* layout, int H, int nb, int nbk, int batch, int order,
+                       bsa_lut** out) {
   if (out == nullptr) return BSA_ERR_NULL;
   *out = nullptr;
   if (layout == nullptr) return BSA_ERR_NULL;
-  // nb < 2^15: the device work-list record packs a row's count and diagonal position
-  // into 16 bits each.
-  if (H < 1 || nb < 1 || nb > 32767 || batch < 1) return BSA_ERR_SHAPE;
-  const int64_t cells = static_cast<int64_t>(H) * nb * nb;
+  // nb, nbk < 2^15: the device work-list record packs a row's count and diagonal
+  // position into 16 bits each.
+  if (H < 1 || nb < 1 || nb > 32767 || nbk < 1 || nbk > 32767 || batch < 1) return BSA_ERR_SHAPE;
+  const int64_t cells = static_cast<int64_t>(H) * nb * nbk;
   const int64_t n_items = static_cast<int64_t>(batch) * H * nb;
   if (cells > kInt32Max || n_items > kInt32Max) return BSA_ERR_SHAPE;
   if (order != BSA_ORDER_GLOBAL && order != BSA_ORDER_GROUPED) return BSA_ERR_UNSUPPORTED;
@@ -194,25 +215,27 @@ int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bs
   try {
     lut->H = H;
     lut->nb = nb;
+    lut->nbk = nbk;
     lut->batch = batch;
     lut->order = order;
     const int rows = H * nb;
     lut->row_ptr.assign(rows + 1, 0);
     for (int r = 0; r < rows; ++r) {
-      const int32_t* lr = layout + static_cast<int64_t>(r) * nb;
+      const int32_t* lr = layout + static_cast<int64_t>(r) * nbk;
       int cnt = 0;
-      for (int j = 0; j < nb; ++j) cnt += lr[j];
+      for (int j = 0; j < nbk; ++j) cnt += lr[j];
       lut->row_ptr[r + 1] = lut->row_ptr[r] + cnt;
     }
     lut->nnz_total = lut->row_ptr[rows];
     lut->col_idx.resize(lut->nnz_total);
     for (int r = 0; r < rows; ++r) {
-      const int32_t* lr = layout + static_cast<int64_t>(r) * nb;
+      const int32_t* lr = layout + static_cast<int64_t>(r) * nbk;
       int32_t* dst = lut->col_idx.data() + lut->row_ptr[r];
-      for (int j = 0; j < nb; ++j)
+      for (int j = 0; j < nbk; ++j)
         if (lr[j]) *dst++ = j;
     }
-    // Position of the diagonal block (j == i) inside each row, for the causal mask.
+    // Position of the diagonal block (j == i) inside each row, for the causal mask of the
+    // plain kernels (equal block sizes).
     lut->diag_pos.assign(rows, -1);
     for (int r = 0; r < rows; ++r) {
       const int i = r % nb;
@@ -252,6 +275,12 @@ int bsa_lut_info(const bsa_lut* lut, int* H, int* nb, int* batch, int* nnz_total
   if (batch) *batch = lut->batch;
   if (nnz_total) *nnz_total = lut->nnz_total;
   if (n_items) *n_items = lut->n_items;
+  return BSA_OK;
+}
+
+int bsa_lut_kv_blocks(const bsa_lut* lut, int* nbk) {
+  if (lut == nullptr || nbk == nullptr) return BSA_ERR_NULL;
+  *nbk = lut->nbk;
   return BSA_OK;
 }
 
@@ -346,10 +375,11 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
     return BSA_ERR_NULL;
   if ((block != 64 && block != 128) || (d != 64 && d != 128)) return BSA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return BSA_ERR_UNSUPPORTED;
-  if (B != lut->batch || H != lut->H || L <= 0 || static_cast<int64_t>(lut->nb) * block != L)
+  if (B != lut->batch || H != lut->H || L <= 0 || lut->nbk != lut->nb ||
+      static_cast<int64_t>(lut->nb) * block != L)
     return BSA_ERR_SHAPE;
   const int64_t rows = static_cast<int64_t>(B) * H * L;
-  if (rows > kInt32Max) return BSA_ERR_SHAPE;
+  if (rows > kInt32Max - 128) return BSA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return BSA_ERR_ALIGN;
   if (lut->d_items == nullptr) return BSA_ERR_STATE;
@@ -374,19 +404,85 @@ int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut,
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
   p.expire_site = lut->expire_site;
+  p.Lq = p.Lk = L;
+  p.H = H;
+  p.window_left = p.window_right = -1;
 
   const int grid = lut->sched_grid;  // the schedule uploaded with the LUT
   if (grid <= 0) return BSA_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (block == 128 && d == 128)
-    e = bsa::launch_fwd_b128_d128(p, tq, tk, tv, grid, st);
-  else if (block == 128)
-    e = bsa::launch_fwd_b128_d64(p, tq, tk, tv, grid, st);
-  else if (d == 128)
-    e = bsa::launch_fwd_b64_d128(p, tq, tk, tv, grid, st);
-  else
-    e = bsa::launch_fwd_b64_d64(p, tq, tk, tv, grid, st);
+  const cudaError_t e = bsa::launch_fwd_variant(block, block, d, false, p, tq, tk, tv, grid, st);
+  return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+int bsa_forward_ext(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
+                    float* lse, int B, int H, int Lq, int Lk, int d, float scale, int q_block,
+                    int kv_block, int causal_diag, const bsa_ext_args* ext, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || lut == nullptr || out == nullptr ||
+      lse == nullptr)
+    return BSA_ERR_NULL;
+  bsa_ext_args x{-1, -1, 0.f, nullptr, nullptr, nullptr};
+  if (ext != nullptr) x = *ext;
+  if ((x.q_segment_ids == nullptr) != (x.kv_segment_ids == nullptr)) return BSA_ERR_NULL;
+  if ((q_block != 64 && q_block != 128) || (kv_block != 64 && kv_block != 128) ||
+      (d != 64 && d != 128))
+    return BSA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !std::isfinite(x.softcap) || x.softcap < 0.f)
+    return BSA_ERR_UNSUPPORTED;
+  if (B != lut->batch || H != lut->H || Lq <= 0 || Lk <= 0 ||
+      lut->nb != (Lq + q_block - 1) / q_block || lut->nbk != (Lk + kv_block - 1) / kv_block)
+    return BSA_ERR_SHAPE;
+  const int64_t rows_q = static_cast<int64_t>(B) * H * Lq;
+  const int64_t rows_k = static_cast<int64_t>(B) * H * Lk;
+  if (rows_q > kInt32Max - 128 || rows_k > kInt32Max - 128) return BSA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return BSA_ERR_ALIGN;
+  auto aligned4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+  if (!aligned4(x.sinks) || !aligned4(x.q_segment_ids) || !aligned4(x.kv_segment_ids))
+    return BSA_ERR_ALIGN;
+  const bool plain = q_block == kv_block && Lq == Lk && Lq % q_block == 0 && x.window_left < 0 &&
+                     x.window_right < 0 && x.softcap == 0.f && x.sinks == nullptr &&
+                     x.q_segment_ids == nullptr;
+  if (plain)  // nothing beyond the plain operation: the plain kernel
+    return bsa_forward(q, k, v, lut, out, lse, B, H, Lq, d, scale, q_block, causal_diag, stream);
+  if (lut->d_items == nullptr) return BSA_ERR_STATE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev != lut->device) return BSA_ERR_STATE;
+
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows(&tq, q, rows_q, d, q_block, d / 64) ||
+      !encode_rows(&tk, k, rows_k, d, kv_block, d / 64) ||
+      !encode_rows(&tv, v, rows_k, d, kv_block, d / 64))
+    return BSA_ERR_CUDA;
+  bsa::FwdParams p{};
+  const bool by_head = bsa::schedule_by_head(lut->sched_policy, B, H, Lk, d, dev);
+  p.items = reinterpret_cast<const int4*>(by_head ? lut->d_items_g : lut->d_items);
+  p.cta_start = by_head ? lut->d_sched_start_g : lut->d_sched_start;
+  p.col_idx = lut->d_col_idx;
+  p.out = out;
+  p.lse = lse;
+  p.status = lut->d_status;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.causal_diag = causal_diag != 0;
+  p.wait_limit_ns = lut->wait_limit_ns;
+  p.expire_site = lut->expire_site;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.H = H;
+  p.window_left = x.window_left < 0 ? -1 : x.window_left;
+  p.window_right = x.window_right < 0 ? -1 : x.window_right;
+  if (x.softcap > 0.f) {
+    p.softcap_log2 = static_cast<float>(static_cast<double>(x.softcap) * 1.4426950408889634);
+    p.softcap_inv = static_cast<float>(static_cast<double>(scale) / x.softcap);
+  }
+  p.sinks = x.sinks;
+  p.q_seg = x.q_segment_ids;
+  p.kv_seg = x.kv_segment_ids;
+  const int grid = lut->sched_grid;
+  if (grid <= 0) return BSA_ERR_STATE;
+  const cudaError_t e = bsa::launch_fwd_variant(q_block, kv_block, d, true, p, tq, tk, tv, grid,
+                                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

@@ -10,11 +10,12 @@
 // The look-up table behind the opaque bsa_lut handle of bsa.h.
 struct bsa_lut {
   int H = 0, nb = 0, batch = 0, order = 0;
+  int nbk = 0;  // key blocks per row (nb for a square layout)
   int nnz_total = 0, n_items = 0;
   std::vector<int32_t> row_ptr;  // [H*nb + 1]
   std::vector<int32_t> col_idx;  // [nnz_total]
   std::vector<int32_t> items;    // [n_items][4] = {b, h, i, nnz}
-  std::vector<int32_t> diag_pos; // [H*nb]: index of block i in row (h, i), or -1
+  std::vector<int32_t> diag_pos; // [H*nb]: index of block j == i in row (h, i), or -1
   // Device schedules for `sched_grid` CTAs (built at upload): the work list regrouped
   // so that CTA c takes sched_items[o][sched_start[o][c] .. sched_start[o][c+1]).  o = 0
   // hands items out in work-list order, o = 1 (batch, head) by (batch, head).
@@ -49,6 +50,15 @@ struct FwdParams {
   int causal_diag;
   unsigned long long wait_limit_ns;
   int expire_site;          // wait site that gives up at once (0: none; bsa_debug_expire_wait)
+  int Lq, Lk;               // rows per (batch, head) of Q/O and of K/V
+  // Extended kernels only:
+  int H;                    // heads: a record's bh = b * H + h
+  int window_left, window_right;  // keys c < r - left / c > r + right masked (< 0: no bound)
+  float softcap_log2;       // cap * log2(e); 0: no soft-cap
+  float softcap_inv;        // scale / cap
+  const float* sinks;       // [H] sink logits (natural log units) or null
+  const int32_t* q_seg;     // [B, Lq] or null
+  const int32_t* kv_seg;    // [B, Lk] or null (null exactly when q_seg is)
 };
 
 // Wait-site ids recorded in the status word's low bits.
@@ -70,9 +80,9 @@ void build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int3
                     std::vector<int32_t>& start);
 
 // Device records of a regrouped work list `items` ({b, h, i, nnz} each):
-// {q_blk, kv_blk, first col_idx entry of the row, nnz | (dpos + 1) << 16} with q_blk =
-// (b*H + h)*nb + i, kv_blk = (b*H + h)*nb and dpos the position of block i in row (h, i)
-// (-1 if absent), so the kernel needs no other table to start an item.
+// {b*H + h, i, first col_idx entry of the row, nnz | (dpos + 1) << 16} with dpos the
+// position of block j == i in row (h, i) (-1 if absent), so the kernel needs no other
+// table to start an item.
 void device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
                     std::vector<int32_t>& records);
 
@@ -81,16 +91,36 @@ void device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
 // device `dev`.
 bool schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t d, int dev);
 
-// One launcher per supported (block, head_dim) pair; each lives in its own
-// translation unit so the variants compile in parallel.
-cudaError_t launch_fwd_b128_d128(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                                 const CUtensorMap& v, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_b128_d64(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_b64_d128(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_b64_d64(const FwdParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, int grid, cudaStream_t stream);
+// Launches the forward kernel for (q_block, kv_block, head_dim, ext); the instances live
+// in their own translation units (bsa_fwd_q*_k*_d*.cu) so they compile in parallel.  The
+// plain kernels (ext = false) exist for q_block == kv_block only.
+cudaError_t launch_fwd_variant(int q_block, int kv_block, int d, bool ext, const FwdParams& p,
+                               const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               int grid, cudaStream_t stream);
+cudaError_t launch_fwd_q64_k64_d64(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                  const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_fwd_q64_k64_d128(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                   const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_fwd_q128_k128_d64(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                    const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                    cudaStream_t stream);
+cudaError_t launch_fwd_q128_k128_d128(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                     const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                     cudaStream_t stream);
+cudaError_t launch_fwd_q64_k128_d64(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                   const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_fwd_q64_k128_d128(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                    const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                    cudaStream_t stream);
+cudaError_t launch_fwd_q128_k64_d64(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                   const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_fwd_q128_k64_d128(bool ext, const FwdParams& p, const CUtensorMap& q,
+                                    const CUtensorMap& k, const CUtensorMap& v, int grid,
+                                    cudaStream_t stream);
 
 // One-CTA kernel whose only wait never completes; it must give up after limit_ns.
 cudaError_t launch_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);

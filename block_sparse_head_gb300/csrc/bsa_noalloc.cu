@@ -77,10 +77,11 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
     return BSA_ERR_NULL;
   if ((block != 64 && block != 128) || (d != 64 && d != 128)) return BSA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return BSA_ERR_UNSUPPORTED;
-  if (B != lut->batch || H != lut->H || L <= 0 || static_cast<int64_t>(lut->nb) * block != L)
+  if (B != lut->batch || H != lut->H || L <= 0 || lut->nbk != lut->nb ||
+      static_cast<int64_t>(lut->nb) * block != L)
     return BSA_ERR_SHAPE;
   const int64_t rows = static_cast<int64_t>(B) * H * L;
-  if (rows > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (rows > 0x7fffffffLL - 128) return BSA_ERR_SHAPE;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (!a16(q) || !a16(k) || !a16(v) || !a16(out) || !a16(lse)) return BSA_ERR_ALIGN;
 
@@ -150,15 +151,10 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
   p.causal_diag = causal_diag != 0;
   p.wait_limit_ns = lut->wait_limit_ns;
   p.expire_site = lut->expire_site;
-  cudaError_t e;
-  if (block == 128 && d == 128)
-    e = bsa::launch_fwd_b128_d128(p, tq, tk, tv, grid, st);
-  else if (block == 128)
-    e = bsa::launch_fwd_b128_d64(p, tq, tk, tv, grid, st);
-  else if (d == 128)
-    e = bsa::launch_fwd_b64_d128(p, tq, tk, tv, grid, st);
-  else
-    e = bsa::launch_fwd_b64_d64(p, tq, tk, tv, grid, st);
+  p.Lq = p.Lk = L;
+  p.H = H;
+  p.window_left = p.window_right = -1;
+  const cudaError_t e = bsa::launch_fwd_variant(block, block, d, false, p, tq, tk, tv, grid, st);
   if (e != cudaSuccess) return BSA_ERR_CUDA;
   if (!sync_status) return BSA_OK;
   int32_t word = 0;

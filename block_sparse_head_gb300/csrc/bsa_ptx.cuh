@@ -267,6 +267,19 @@ __device__ __forceinline__ float mask_gt(float x, int k, int lim) {
   return r;
 }
 
+// x if lo <= k <= hi, else -inf, as predicated selects (no branch).
+__device__ __forceinline__ float mask_outside(float x, int k, int lo, int hi) {
+  float r;
+  asm("{\n\t.reg .pred p, q;\n\t"
+      "setp.lt.s32 p, %2, %3;\n\t"
+      "setp.gt.s32 q, %2, %4;\n\t"
+      "or.pred p, p, q;\n\t"
+      "selp.f32 %0, 0fFF800000, %1, p;\n\t}"
+      : "=f"(r)
+      : "f"(x), "r"(k), "r"(lo), "r"(hi));
+  return r;
+}
+
 // 32-byte global store (eight 32-bit words); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,

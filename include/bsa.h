@@ -90,6 +90,21 @@ typedef struct bsa_lut bsa_lut;
 int bsa_build_lut(const int32_t* layout, int H, int nb, int batch, int order, bsa_lut** out);
 
 /*
+ * bsa_build_lut_rect -- bsa_build_lut for a rectangular layout int32 [H, nb, nbk]: nb
+ * query blocks by nbk key blocks per head, as bsa_forward_ext takes when the query and
+ * key block sizes differ or the lengths are not multiples of them (nb = ceil(Lq /
+ * q_block), nbk = ceil(Lk / kv_block); the last block of a ragged sequence is clipped
+ * at its end, as the mask builder of the "Block-Sparse Attention" page, section "Block
+ * Structure", clips it).  Rows are the nb query blocks; col_idx holds key-block
+ * indices in [0, nbk).  1 <= nb, nbk < 2^15.  Errors as bsa_build_lut.
+ */
+int bsa_build_lut_rect(const int32_t* layout, int H, int nb, int nbk, int batch, int order,
+                       bsa_lut** out);
+
+/* bsa_lut_kv_blocks -- key blocks per row (nbk) of a LUT; nb for a square one. */
+int bsa_lut_kv_blocks(const bsa_lut* lut, int* nbk);
+
+/*
  * bsa_lut_info -- sizes of a LUT.  Any output pointer may be NULL.
  * nnz_total = sum of the layout = length of col_idx; n_items = batch*H*nb.
  */
@@ -155,6 +170,59 @@ void bsa_lut_free(bsa_lut* lut);
 int bsa_forward(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
                 float* lse, int B, int H, int L, int d, float scale, int block, int causal_diag,
                 void* stream);
+
+/*
+ * Per-element predicates and extra terms of bsa_forward_ext.  They follow the argument
+ * list of ejkernel's blocksparse_attention ("sliding_window" as a (left, right) pair,
+ * "logits_soft_cap", "softmax_aux" for attention sinks, query / key-value segment ids)
+ * and the sink term of the DeepSeek-V4.1 sparse_attn kernel ("Sparse attention /
+ * Weighted row sum").  A zeroed struct with both window sides set to -1 (or a NULL
+ * pointer) means none of them.
+ */
+typedef struct bsa_ext_args {
+  int window_left;               /* key c masked when c < r - window_left; < 0: no bound  */
+  int window_right;              /* key c masked when c > r + window_right; < 0: no bound */
+  float softcap;                 /* > 0: each scaled score s becomes softcap*tanh(s /
+                                    softcap); 0: off                                       */
+  const float* sinks;            /* device fp32 [H] or NULL: head h's sink logit t_h adds
+                                    exp(t_h) to the softmax normaliser (no value row), so
+                                    lse includes it and an empty row gets lse = t_h        */
+  const int32_t* q_segment_ids;  /* device int32 [B, Lq] or NULL                          */
+  const int32_t* kv_segment_ids; /* device int32 [B, Lk] or NULL (both or neither): key c
+                                    is masked for query r when their ids differ            */
+} bsa_ext_args;
+
+/*
+ * bsa_forward_ext -- bsa_forward with ragged lengths, different query and key block
+ * sizes, and the predicates of bsa_ext_args.  For batch b, head h, query row r in
+ * [0, Lq):
+ *
+ *   A(r) = { c in [0, Lk) : layout[h][r/q_block][c/kv_block] == 1, not masked by the
+ *            window or the segment ids, and not (causal_diag && c > r && key block
+ *            c/kv_block overlaps the rows of query block r/q_block) }
+ *   s_c  = scale * <q[b,h,r,:], k[b,h,c,:]>, then softcap*tanh(s_c/softcap) if set
+ *   lse[r] = ln( sum_{c in A(r)} exp(s_c) + exp(sinks[h]) if sinks )  (-inf if empty)
+ *   O[r,:] = sum_{c in A(r)} exp(s_c - lse[r]) v[b,h,c,:]            (0 if A(r) empty)
+ *
+ * The diagonal mask reads "diagonal block" as every key block whose key range overlaps
+ * the query block's rows (the block j == i when the sizes are equal).
+ *
+ *   q, out   device bf16 [B,H,Lq,d];  k, v  device bf16 [B,H,Lk,d]  (16-byte aligned).
+ *   lse      device fp32 [B,H,Lq].
+ *   lut      uploaded LUT of layout [H, ceil(Lq/q_block), ceil(Lk/kv_block)]
+ *            (bsa_build_lut_rect; bsa_build_lut when both are nb).
+ *   q_block, kv_block  64 or 128 each;  d 64 or 128.
+ *   ext      predicates (NULL: none); its device arrays 4-byte aligned.
+ *
+ * With equal blocks, Lq == Lk a multiple of the block and no predicate this is exactly
+ * bsa_forward (the same kernel).  Asynchronous, no allocation, one kernel launch.
+ * Errors: BSA_ERR_NULL (also: exactly one segment array given), BSA_ERR_SHAPE,
+ * BSA_ERR_ALIGN, BSA_ERR_UNSUPPORTED (block or head dim, non-finite scale, negative or
+ * non-finite softcap), BSA_ERR_STATE, BSA_ERR_CUDA.
+ */
+int bsa_forward_ext(const void* q, const void* k, const void* v, const bsa_lut* lut, void* out,
+                    float* lse, int B, int H, int Lq, int Lk, int d, float scale, int q_block,
+                    int kv_block, int causal_diag, const bsa_ext_args* ext, void* stream);
 
 /*
  * bsa_forward_noalloc -- the same forward as bsa_forward for callers that cannot

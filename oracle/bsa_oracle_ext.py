@@ -53,6 +53,33 @@ def n_blocks(length: int, block: int) -> int:
     return -(-length // block)
 
 
+def lut_rect(layout, batch: int, order: str = "global"):
+    """CSR + work list of a rectangular layout [H, nbq, nbk], by the same definition as
+    ``bsa_oracle.oracle_lut`` (rows are the query blocks h * nbq + i, columns the active
+    key blocks ascending; items {b, h, i, nnz} sorted by (-nnz, b, h, i) or
+    (b, h, -nnz, i))."""
+    lay = np.asarray(layout)
+    if lay.ndim != 3 or not np.isin(lay, (0, 1)).all():
+        raise ValueError("layout must be [H, nbq, nbk] of 0/1")
+    H, nbq, _ = lay.shape
+    row_ptr, col_idx, items = [0], [], []
+    for h in range(H):
+        for i in range(nbq):
+            cols = [int(j) for j in np.nonzero(lay[h, i] == 1)[0]]
+            col_idx.extend(cols)
+            row_ptr.append(row_ptr[-1] + len(cols))
+    for b in range(batch):
+        for h in range(H):
+            for i in range(nbq):
+                r = h * nbq + i
+                items.append((b, h, i, row_ptr[r + 1] - row_ptr[r]))
+    key = (lambda t: (-t[3], t[0], t[1], t[2])) if order == "global" else \
+        (lambda t: (t[0], t[1], -t[3], t[2]))
+    items.sort(key=key)
+    return (np.asarray(row_ptr, np.int32), np.asarray(col_idx, np.int32),
+            np.asarray(items, np.int32).reshape(-1, 4))
+
+
 def element_mask(layout_h, Lq: int, Lk: int, q_block: int, kv_block: int, causal_diag: bool,
                  window_left: int = -1, window_right: int = -1, q_seg=None, kv_seg=None):
     """Boolean [Lq, Lk] mask of one (batch, head): A(r) of every row r."""

@@ -190,3 +190,51 @@ def test_schedule_policy_validation(lib):
         lut.set_schedule(policy)
     assert lib.bsa_set_schedule(lut.handle, 3) == -6   # BSA_ERR_UNSUPPORTED
     assert lib.bsa_set_schedule(None, 0) == -1         # BSA_ERR_NULL
+
+
+# ------------------------------------------------ rectangular layouts (bsa_build_lut_rect)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_rect_lut_bit_exact(lib, seed):
+    from oracle import bsa_oracle_ext as ox
+
+    rng = np.random.default_rng(100 + seed)
+    H, nbq, nbk, B = (int(rng.integers(1, 4)), int(rng.integers(1, 12)), int(rng.integers(1, 12)),
+                      int(rng.integers(1, 3)))
+    lay = (rng.random((H, nbq, nbk)) < rng.uniform(0.1, 0.9)).astype(np.int32)
+    lay[:, rng.integers(0, nbq)] = 0  # an empty row
+    for order in ("global", "grouped"):
+        lut = bsa.build_lut(lay, B, order, upload=False)
+        assert (lut.nb, lut.nbk) == (nbq, nbk)
+        rp, ci, it = lut.export()
+        orp, oci, oit = ox.lut_rect(lay, B, order)
+        assert np.array_equal(rp, orp) and np.array_equal(ci, oci) and np.array_equal(it, oit)
+
+
+def test_rect_lut_oracle_matches_square_oracle():
+    from oracle import bsa_oracle_ext as ox
+
+    lay = wls.random_layout(3, 9, 0.4, 8, empty_rows=2).numpy()
+    for order in ("global", "grouped"):
+        for a, b in zip(ox.lut_rect(lay, 2, order), oracle.oracle_lut(lay, 2, order)):
+            assert np.array_equal(a, b)
+
+
+def test_forward_ext_validation(lib):
+    """Argument errors of bsa_forward_ext come back before any device work."""
+    lay = np.ones((2, 3, 5), np.int32)  # Lq = 3 query blocks of 128, Lk = 5 key blocks of 64
+    lut = bsa.build_lut(lay, 1, upload=False)
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced
+
+    def call(Lq=300, Lk=300, qb=128, kb=64, ext=None, d=128):
+        return lib.bsa_forward_ext(fake, fake, fake, lut.handle, fake, fake, 1, 2, Lq, Lk, d,
+                                   ctypes.c_float(0.1), qb, kb, 1,
+                                   None if ext is None else ctypes.byref(ext), None)
+
+    seg = binding.ExtArgs(-1, -1, 0.0, None, 1 << 20, None)
+    assert call(ext=seg) == -1                                 # one segment array only
+    assert call(kb=32) == -6 and call(d=96) == -6              # unsupported sizes
+    assert call(ext=binding.ExtArgs(-1, -1, -1.0, None, None, None)) == -6  # negative softcap
+    assert call(Lk=400) == -2 and call(Lq=500) == -2           # layout / length mismatch
+    assert call() == -9                                        # valid, but never uploaded
