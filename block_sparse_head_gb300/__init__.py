@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     BSA_ORDER_GROUPED,
     BsaError,
     Lut,
+    backward,
     build_lut,
     forward,
     forward_ext,

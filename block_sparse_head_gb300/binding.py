@@ -30,7 +30,8 @@ EXPORTED = (
     "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
     "bsa_wait_selftest",
     "bsa_status_string", "bsa_version", "bsa_forward_noalloc", "bsa_debug_expire_wait",
-    "bsa_build_lut_rect", "bsa_lut_kv_blocks", "bsa_forward_ext",
+    "bsa_build_lut_rect", "bsa_lut_kv_blocks", "bsa_forward_ext", "bsa_lut_export_csc",
+    "bsa_backward",
 )
 
 
@@ -79,6 +80,10 @@ def load_library():
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(ExtArgs), vp]
+        lib.bsa_lut_export_csc.argtypes = [vp, vp, vp, vp]
+        lib.bsa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_int, ctypes.c_int, vp]
         lib.bsa_lut_info.argtypes = [vp, ip, ip, ip, ip, ip]
         lib.bsa_lut_export.argtypes = [vp, vp, vp, vp]
         lib.bsa_lut_schedule.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
@@ -105,7 +110,8 @@ def load_library():
                      "bsa_lut_upload",
                      "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
                      "bsa_wait_selftest", "bsa_debug_expire_wait", "bsa_build_lut_rect",
-                     "bsa_lut_kv_blocks", "bsa_forward_ext"):
+                     "bsa_lut_kv_blocks", "bsa_forward_ext", "bsa_lut_export_csc",
+                     "bsa_backward"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -156,6 +162,15 @@ class Lut:
         _check(self._lib.bsa_lut_export(self.handle, rp.ctypes.data, ci.ctypes.data, it.ctypes.data),
                "bsa_lut_export")
         return rp, ci[:self.nnz_total], it
+
+    def export_csc(self):
+        """(col_ptr [H*nb+1], row_idx [nnz], items [n_items, 4]) of the column view."""
+        cp = np.empty(self.H * self.nb + 1, np.int32)
+        ri = np.empty(max(self.nnz_total, 1), np.int32)
+        it = np.empty((self.n_items, 4), np.int32)
+        _check(self._lib.bsa_lut_export_csc(self.handle, cp.ctypes.data, ri.ctypes.data,
+                                            it.ctypes.data), "bsa_lut_export_csc")
+        return cp, ri[:self.nnz_total], it
 
     def schedule(self, grid: int, by_head: bool = False):
         """(items [n_items, 4], cta_start [grid + 1]) of the per-CTA schedule for ``grid``
@@ -282,6 +297,33 @@ def forward_ext(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, sca
                                int(q_block), int(kv_block), int(bool(causal_diag)),
                                ctypes.byref(x), _stream_handle(stream)), "bsa_forward_ext")
     return out, lse
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, lut: Lut, scale: float, block: int,
+             causal_diag: bool, dq=None, dk=None, dv=None, delta=None, stream=None):
+    """Gradients (dq, dk, dv) of the forward (bsa_backward).  q, k, v, out, dout: bf16
+    [B, H, L, d] on the LUT's device; lse fp32 [B, H, L] from the forward.  ``delta`` is
+    an fp32 [B, H, L] workspace (allocated when None)."""
+    lib = load_library()
+    B, H, L, d = q.shape
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check_qkv(t, name, (B, H, L, d))
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, L) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, L] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_qkv(t, name, (B, H, L, d))
+    if delta is None:
+        delta = torch.empty(B, H, L, device=q.device, dtype=torch.float32)
+    _check(lib.bsa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), dout.data_ptr(), lut.handle, dq.data_ptr(),
+                            dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, L, d,
+                            float(scale), int(block), int(bool(causal_diag)),
+                            _stream_handle(stream)), "bsa_backward")
+    return dq, dk, dv
 
 
 def forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: float,

@@ -1,0 +1,467 @@
+// bsa_bwd_kernel.cuh -- block-sparse attention backward for sm_103a: dQ over the layout's
+// rows, dK and dV over its columns.
+//
+// Method.  With P the masked softmax of the forward (recomputed from Q, K and the
+// forward's lse, so P = exp(scale * q.k - lse) on active entries and 0 elsewhere) and
+// delta[r] = sum_x dO[r,x] O[r,x]:
+//     dP = dO V^T,  dS = P * (dP - delta),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// Masked entries have P = 0, so only the active blocks pass gradient ("Block Sparse
+// Attention Techniques", section 2, "Gradient Propagation in Block Sparse Attention").
+//
+// One kernel template, two modes over the same pipeline:
+//   dQ mode (KV = false): a work item is a query block i of one (batch, head) and walks
+//     the key blocks j of its CSR row.  Item tiles A = Q_i, B = dO_i; step tiles X = K_j,
+//     Y = V_j.  T1 = A X^T = S, T2 = B Y^T = dP; E1 = dS;  acc1 += E1 X = dQ / scale.
+//   dK/dV mode (KV = true): a work item is a key block j and walks the query blocks i of
+//     its CSC column.  Item tiles A = K_j, B = V_j; step tiles X = Q_i, Y = dO_i (plus
+//     the lse and delta of those query rows).  T1 = A X^T = S^T, T2 = B Y^T = dP^T;
+//     E1 = P^T, E2 = dS^T;  acc1 += E1 Y = dV,  acc2 += E2 X = dK / scale.
+// A step covers 128 columns: one block when b = 128, two when b = 64.
+//
+// GB300 mapping.  One CTA per SM, persistent over its share of the work list (the same
+// longest-first per-CTA schedule as the forward):
+//   warp 0      TMA producer: item tiles (one 3-D copy each) and step tiles into two
+//               stages; in dK/dV mode also the step's lse and delta (bulk copies).
+//   warp 1      MMA issuer (one thread) and TMEM owner: T1 (128 columns), T2 (128), acc1
+//               (d) and, in dK/dV mode, acc2 (d) -- 512 columns at d = 128.
+//   warps 2..   elementwise warpgroups (two at b = 128, one at b = 64), laid out as the
+//               forward's softmax: per step they read T1 and T2, form P and dS, and write
+//               the bf16 operands E1 (over T1) and E2 (over T2) for the second MMAs.  At an
+//               item's end they read the accumulators, scale and store them as bf16.
+// Each step runs MMA1/MMA2 -> elementwise -> MMA3/MMA4 in order (T1/T2 are single
+// buffered); the step tiles of the next step load meanwhile.  Every wait is bounded
+// (WaitCtl), as in the forward.
+#pragma once
+
+#include "bsa_fwd_kernel.cuh"
+
+namespace bsa {
+
+template <int BLK, int D, bool KV>
+struct BwdCfg {
+  static_assert(BLK == 64 || BLK == 128, "block must be 64 or 128");
+  static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+  static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // elementwise warpgroups
+  static constexpr int kEwWarps = 4 * kNumWG;
+  static constexpr int kThreads = 32 * (2 + kEwWarps);
+  static constexpr int kG = 128 / BLK;           // column blocks per step
+  static constexpr int kItemTile = BLK * D * 2;  // one item tile (A or B)
+  static constexpr int kStepTile = 128 * D * 2;  // one step tile (X or Y), kG blocks
+  static constexpr int kBlkB = BLK * D * 2;      // one block of a step tile
+  static constexpr int kHalf = BLK * 128;        // one 64-column half of one block
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kItemTile;
+  static constexpr int kOffX = 2 * kItemTile;            // [2] stages
+  static constexpr int kOffY = kOffX + 2 * kStepTile;    // [2] stages
+  static constexpr int kOffVec = kOffY + 2 * kStepTile;  // [2] stages x {lse, delta}[128] fp32
+  static constexpr int kVecBytes = KV ? 2 * 2 * 128 * 4 : 0;
+  static constexpr int kOffBar = kOffVec + kVecBytes;
+  // barriers
+  static constexpr int kBarIF = 0;    // item tiles landed
+  static constexpr int kBarIE = 1;    // item tiles free (the item's last MMA1/MMA2 done)
+  static constexpr int kBarXF = 2;    // [2] step tiles landed
+  static constexpr int kBarXE = 4;    // [2] step tiles free (the step's MMA3/MMA4 done)
+  static constexpr int kBarTF = 6;    // T1, T2 computed
+  static constexpr int kBarEF = 7;    // E1 (E2) written (one arrive per elementwise warp)
+  static constexpr int kBarAD = 8;    // the step's MMA3/MMA4 done
+  static constexpr int kBarAR = 9;    // accumulators read out (one arrive per elementwise warp)
+  static constexpr int kBarDrain = 10;
+  static constexpr int kNumBars = 11;
+  static constexpr int kBarBytes = 128;  // barriers, TMEM slot, abort flag
+  static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr int kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
+  // TMEM columns
+  static constexpr int kT1 = 0, kT2 = 128, kAcc1 = 256, kAcc2 = 256 + D;
+  static_assert(kAcc2 + (KV ? D : 0) <= 512, "TMEM budget");
+  static constexpr uint32_t kIdesc1 = idesc_bf16_f32(BLK, 128, false, false);  // N = 128
+  static constexpr uint32_t kIdesc1b = idesc_bf16_f32(BLK, BLK, false, false); // one block
+  static constexpr uint32_t kIdesc3 = idesc_bf16_f32(BLK, D, false, true);     // B MN-major
+};
+
+// Stores this thread's packed columns of one row (the read_o layout) as bf16.
+template <int D>
+__device__ __forceinline__ void store_row_bf16(void* base, int row, int half,
+                                               const uint32_t (&pk)[D / 4]) {
+  constexpr int OC = D / 2;
+  __nv_bfloat16* r = static_cast<__nv_bfloat16*>(base) + static_cast<size_t>(row) * D + half * 32;
+#pragma unroll
+  for (int q = 0; q < OC / 8; ++q)  // 8 columns per store; group q / 4
+    *reinterpret_cast<uint4*>(r + (q >> 2) * 64 + (q & 3) * 8) =
+        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+template <int D>
+__device__ __forceinline__ void zero_row_bf16(void* base, int row, int half) {
+  constexpr int OC = D / 2;
+  uint4* r = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) +
+                                      static_cast<size_t>(row) * D + half * OC);
+#pragma unroll
+  for (int c = 0; c < OC / 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
+}
+
+// ----------------------------------------------------------------- producer
+
+template <int BLK, int D, bool KV>
+__device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorMap* tm_a,
+                                             const CUtensorMap* tm_b, const CUtensorMap* tm_x,
+                                             const CUtensorMap* tm_y, uint32_t sbase,
+                                             const WaitCtl& ctl) {
+  using C = BwdCfg<BLK, D, KV>;
+  constexpr int G = C::kG;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  StepCursor<G> c;
+  c.init(p);
+  int n = -1, t = 0;
+  bool ok = true;
+  for (; c.valid(); ++t) {
+    const int nblk = c.nblk();
+    const int bh = c.is.cur.x;
+    int cols[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) cols[g] = (g < nblk) ? p.col_idx[c.is.cur.z + c.s * G + g] : 0;
+    if (c.s == 0) {
+      // Item tiles: one buffer, free once the previous item's last MMA1/MMA2 completed.
+      // n counts the items whose tiles were armed.
+      if (n >= 0 && !mbar_wait(bar(C::kBarIE), n & 1, ctl, kSiteProdKEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = bar(C::kBarIF);
+      mbar_arrive_expect_tx(fb, 2 * C::kItemTile);
+      ++n;
+      const int row = bh * p.L + c.is.cur.y * BLK;
+      tma_load_3d(sbase + C::kOffA, tm_a, fb, 0, row, 0);
+      tma_load_3d(sbase + C::kOffB, tm_b, fb, 0, row, 0);
+    }
+    c.advance(p);
+    // Step stage t % 2 held step t-2, read by its MMA3/MMA4.
+    if (t >= 2 && !mbar_wait(bar(C::kBarXE + t % 2), ((t - 2) / 2) & 1, ctl, kSiteProdVEmpty)) {
+      ok = false;
+      break;
+    }
+    const uint32_t fb = bar(C::kBarXF + t % 2);
+    mbar_arrive_expect_tx(fb, nblk * (2 * C::kBlkB + (KV ? 2 * BLK * 4 : 0)));
+    const uint32_t xd = sbase + C::kOffX + (t % 2) * C::kStepTile;
+    const uint32_t yd = sbase + C::kOffY + (t % 2) * C::kStepTile;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (g < nblk) {
+        const int row = bh * p.L + cols[g] * BLK;
+        tma_load_3d(xd + g * C::kBlkB, tm_x, fb, 0, row, 0);
+        tma_load_3d(yd + g * C::kBlkB, tm_y, fb, 0, row, 0);
+        if constexpr (KV) {
+          const uint32_t vd = sbase + C::kOffVec + (t % 2) * 1024 + g * BLK * 4;
+          bulk_load(vd, p.lse + row, BLK * 4, fb);
+          bulk_load(vd + 512, p.delta + row, BLK * 4, fb);
+        }
+      }
+    }
+  }
+  (void)ok;
+  // Wait for every copy this thread issued (immediate on the normal path).
+  for (int j = (t > 2 ? t - 2 : 0); j < t; ++j) mbar_drain_wait(bar(C::kBarXF + j % 2), (j / 2) & 1);
+  if (n >= 0) mbar_drain_wait(bar(C::kBarIF), n & 1);
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+template <int BLK, int D, bool KV>
+__device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                        const WaitCtl& ctl) {
+  using C = BwdCfg<BLK, D, KV>;
+  constexpr int G = C::kG;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  // Descriptor low words (start address >> 4 and the leading offset); the high word
+  // (stride 1024, version, 128-byte swizzle) is shared.  K-major for the first MMAs,
+  // MN-major (columns d contiguous, halves kHalf apart) for the step tiles as B of the
+  // second ones.
+  const uint64_t a_desc = sdesc_sw128(sbase + C::kOffA, 16, 1024);
+  const uint32_t hi = static_cast<uint32_t>(a_desc >> 32);
+  const uint32_t a0 = static_cast<uint32_t>(a_desc);
+  const uint32_t b0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffB, 16, 1024));
+  const uint32_t x0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffX, 16, 1024));
+  const uint32_t y0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, 16, 1024));
+  const uint32_t xm0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffX, C::kHalf, 1024));
+  const uint32_t ym0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, C::kHalf, 1024));
+  constexpr uint32_t kStage = C::kStepTile >> 4;
+  const uint32_t t1 = tmem + C::kT1, t2 = tmem + C::kT2;
+  const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
+
+  StepCursor<G> c;
+  c.init(p);
+  int n = -1;
+  for (int t = 0; c.valid(); ++t) {
+    const int nblk = c.nblk();
+    const bool first = c.s == 0;
+    const bool last = c.s == c.nsteps - 1;
+    c.advance(p);
+    if (first) {
+      ++n;
+      if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) break;
+    }
+    if (!mbar_wait(bar(C::kBarXF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) break;
+    // T1/T2 are free once the previous step's MMA3/MMA4 have read E1/E2 from them.
+    if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
+    tc_fence_after();
+    const uint32_t xs = x0 + (t % 2) * kStage, ys = y0 + (t % 2) * kStage;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
+      const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
+      if (BLK == 128) {
+        tc_mma_ss_lh(t1, a0 + ia, hi, xs + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+        tc_mma_ss_lh(t2, b0 + ia, hi, ys + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < nblk) {
+            const uint32_t go = (g * C::kBlkB) >> 4;
+            tc_mma_ss_lh(t1 + g * BLK, a0 + ia, hi, xs + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
+            tc_mma_ss_lh(t2 + g * BLK, b0 + ia, hi, ys + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
+          }
+      }
+    }
+    tc_commit(bar(C::kBarTF));
+    if (last) tc_commit(bar(C::kBarIE));
+    if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
+    // An item's first accumulation overwrites the accumulators: the previous item's must
+    // have been read out.
+    if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+    tc_fence_after();
+    const uint32_t xm = xm0 + (t % 2) * kStage, ym = ym0 + (t % 2) * kStage;
+    const int ksteps = nblk * BLK / 16;
+#pragma unroll
+    for (int kk = 0; kk < 128 / 16; ++kk) {
+      if (kk < ksteps) {
+        const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+        const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+        if constexpr (KV) {
+          tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
+          tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
+        } else {
+          tc_mma_ts_lh(acc1, t1 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dQ += dS K
+        }
+      }
+    }
+    tc_commit(bar(C::kBarAD));
+    tc_commit(bar(C::kBarXE + t % 2));
+  }
+  tc_commit(bar(C::kBarDrain));
+  mbar_drain_wait(bar(C::kBarDrain), 0);
+}
+
+// ----------------------------------------------------------- elementwise warps
+
+template <int BLK, int D, bool KV>
+__device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                                const WaitCtl& ctl) {
+  using C = BwdCfg<BLK, D, KV>;
+  constexpr int G = C::kG;
+  constexpr float kLog2e = 1.4426950408889634f;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const int wg = ((threadIdx.x >> 5) - 2) >> 2;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int row = (BLK == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
+  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (BLK == 128 ? wg * 16 : 0)) << 16);
+  const int kbase = (BLK == 128) ? 64 * half : 0;  // first column of this half in its block
+  const float* vec = reinterpret_cast<const float*>(
+      __cvta_shared_to_generic(sbase + C::kOffVec));  // KV: [stage][lse | delta][128]
+
+  auto warp_arrive = [&](int b) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(b));
+  };
+  auto wait_bar = [&](int b, int parity, int site) -> bool {
+    bool w = mbar_wait(bar(b), parity, ctl, site);
+    w = __all_sync(0xffffffffu, w);
+    if (w) tc_fence_after();
+    return w;
+  };
+
+  int g = 0;
+  ItemStream is;
+  for (is.init<false>(p); !is.done(); is.next<false>(p)) {
+    const int cnt = is.nnz();
+    const int orow = is.cur.x * p.L + is.cur.y * BLK + row;  // this thread's output row
+    if (cnt == 0) {
+      zero_row_bf16<D>(p.out1, orow, half);
+      if (KV) zero_row_bf16<D>(p.out2, orow, half);
+      continue;
+    }
+    float lr = 0.f, dr = 0.f;  // dQ mode: this row's lse (log2 units) and delta
+    if constexpr (!KV) {
+      lr = p.lse[orow] * kLog2e;
+      dr = p.delta[orow];
+    }
+    const int dpos = p.causal_diag ? is.dpos() : -1;
+    const int nsteps = (cnt + G - 1) / G;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s, ++g) {
+      const int nblk = step_blocks<G>(cnt, s);
+      const bool valid = (BLK == 128) || (half < nblk);
+      const bool diag = valid && (((BLK == 128) ? s : s * 2 + half) == dpos);
+      if (!wait_bar(C::kBarTF, g & 1, kSiteSoftSFull)) {
+        ok = false;
+        break;
+      }
+      uint32_t rs[64], rp[64];
+      tmem_ld_16x32bx2_x32<64>(tl + C::kT1, *reinterpret_cast<uint32_t(*)[32]>(rs));
+      tmem_ld_16x32bx2_x32<64>(tl + C::kT1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+      tmem_ld_16x32bx2_x32<64>(tl + C::kT2, *reinterpret_cast<uint32_t(*)[32]>(rp));
+      tmem_ld_16x32bx2_x32<64>(tl + C::kT2 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp));
+      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+      // Masked columns: the diagonal block's entries above the diagonal (dQ: key after
+      // the query; dK/dV: query before the key).
+      const int lo = (KV && diag) ? row - kbase : -(1 << 30);
+      const int hi = (!KV && diag) ? row - kbase : (1 << 30);
+      uint32_t pk1[32], pk2[32];
+      const float* vl = vec + (g % 2) * 256 + 64 * half;  // KV: this half's lse ...
+      const float* vd = vl + 128;                         // ... and delta
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float e[2], ds[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cc = 2 * i + u;
+          const float l2 = KV ? vl[cc] * kLog2e : lr;
+          const float dd = KV ? vd[cc] : dr;
+          // masked after scaling, so that a negative scale cannot turn -inf into +inf
+          const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - l2, cc, lo, hi);
+          const float pe = valid ? ex2_approx(y) : 0.f;
+          e[u] = pe;
+          ds[u] = valid ? pe * (__uint_as_float(rp[cc]) - dd) : 0.f;
+        }
+        pk1[i] = pack_bf16x2(KV ? e[0] : ds[0], KV ? e[1] : ds[1]);
+        pk2[i] = pack_bf16x2(ds[0], ds[1]);
+      }
+      tmem_st_16x32bx2_x32<32>(tl + C::kT1, pk1);
+      if constexpr (KV) tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
+      tmem_st_wait();
+      warp_arrive(C::kBarEF);
+    }
+    if (!ok) break;
+    // The item's accumulators are complete once its last step's MMA3/MMA4 are.
+    if (!wait_bar(C::kBarAD, (g - 1) & 1, kSiteSoftItemDone)) break;
+    uint32_t pk[D / 4];
+    read_o<D>(tl + C::kAcc1, KV ? 1.f : p.scale, pk);
+    if constexpr (KV) {
+      uint32_t pk2[D / 4];
+      read_o<D>(tl + C::kAcc2, p.scale, pk2);
+      warp_arrive(C::kBarAR);
+      store_row_bf16<D>(p.out1, orow, half, pk);
+      store_row_bf16<D>(p.out2, orow, half, pk2);
+    } else {
+      warp_arrive(C::kBarAR);
+      store_row_bf16<D>(p.out1, orow, half, pk);
+    }
+  }
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int BLK, int D, bool KV>
+__global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
+    bsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                   const BwdParams p) {
+  using C = BwdCfg<BLK, D, KV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + C::kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+    for (int i = 0; i < C::kNumBars; ++i)
+      mbar_init(bar(i), (i == C::kBarEF || i == C::kBarAR) ? C::kEwWarps : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, p.expire_site};
+  if (warp == 0) {
+    if (lane == 0) bwd_producer<BLK, D, KV>(p, &tm_a, &tm_b, &tm_x, &tm_y, sbase, ctl);
+  } else if (warp == 1) {
+    if (lane == 0) bwd_mma<BLK, D, KV>(p, sbase, tmem, ctl);
+  } else {
+    bwd_elementwise<BLK, D, KV>(p, sbase, tmem, ctl);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int BLK, int D, bool KV>
+cudaError_t launch_bwd(const BwdParams& p, const CUtensorMap& a, const CUtensorMap& b,
+                       const CUtensorMap& x, const CUtensorMap& y, int grid, cudaStream_t stream) {
+  using C = BwdCfg<BLK, D, KV>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(bsa_bwd_kernel<BLK, D, KV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
+  bsa_bwd_kernel<BLK, D, KV><<<grid, C::kThreads, C::kLaunchSmem, stream>>>(a, b, x, y, p);
+  return cudaGetLastError();
+}
+
+// delta[r] = sum_x dO[r,x] O[r,x] (fp32), D/8 lanes per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bsa_bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                            const __nv_bfloat16* __restrict__ dout,
+                                                            float* __restrict__ delta, int rows) {
+  constexpr int R = D / 8;  // lanes per row
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / R;
+  float acc = 0.f;
+  if (r < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + r * D + (lane % R) * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + r * D + (lane % R) * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa = __bfloat1622float2(a2[i]);
+      const float2 fb = __bfloat1622float2(b2[i]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int w = R / 2; w >= 1; w /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+  if (r < rows && lane % R == 0) delta[r] = acc;
+}
+
+}  // namespace bsa

@@ -154,12 +154,14 @@ struct ItemStream {
   int4 nx1;
   int4 nx2;
 
-  __device__ __forceinline__ int4 fetch(const FwdParams& p, int u) const {
+  // P: any kernel-argument struct with `items` and `cta_start` (forward or backward).
+  template <class P>
+  __device__ __forceinline__ int4 fetch(const P& p, int u) const {
     return u < end ? p.items[u] : make_int4(0, 0, 0, -1);
   }
   // Moves to the next item (kSkipEmpty: the next one with active blocks).
-  template <bool kSkipEmpty>
-  __device__ __forceinline__ void next(const FwdParams& p) {
+  template <bool kSkipEmpty, class P>
+  __device__ __forceinline__ void next(const P& p) {
     for (;;) {
       ++t;
       cur = nx1;
@@ -169,8 +171,8 @@ struct ItemStream {
       if (!kSkipEmpty || cur.w != 0) return;
     }
   }
-  template <bool kSkipEmpty>
-  __device__ __forceinline__ void init(const FwdParams& p) {
+  template <bool kSkipEmpty, class P>
+  __device__ __forceinline__ void init(const P& p) {
     t = p.cta_start[blockIdx.x] - 1;
     end = p.cta_start[blockIdx.x + 1];
     n = -1;
@@ -188,12 +190,14 @@ template <int G>
 struct StepCursor {
   ItemStream is;
   int s, nsteps;
-  __device__ __forceinline__ void init(const FwdParams& p) {
+  template <class P>
+  __device__ __forceinline__ void init(const P& p) {
     is.init<true>(p);
     s = 0;
     nsteps = is.done() ? 0 : (is.nnz() + G - 1) / G;
   }
-  __device__ __forceinline__ void advance(const FwdParams& p) {
+  template <class P>
+  __device__ __forceinline__ void advance(const P& p) {
     if (++s >= nsteps) {
       is.next<true>(p);
       s = 0;

@@ -87,11 +87,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // within each pair: the CTAs then work on a few pairs at a time, whose K and V stay in L2.
 void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                          std::vector<int32_t>& start) {
-  const int n = lut.n_items;
+  build_schedule_list(lut.items, grid, by_head, items, start);
+}
+
+void bsa::build_schedule_list(const std::vector<int32_t>& list, int grid, bool by_head,
+                              std::vector<int32_t>& items, std::vector<int32_t>& start) {
+  const int n = static_cast<int>(list.size() / 4);
   std::vector<int32_t> order(static_cast<size_t>(n));
   for (int k = 0; k < n; ++k) order[static_cast<size_t>(k)] = k;
   if (by_head) {
-    const int32_t* it = lut.items.data();
+    const int32_t* it = list.data();
     std::stable_sort(order.begin(), order.end(), [it](int32_t a, int32_t b) {
       const int32_t* x = it + 4 * static_cast<size_t>(a);
       const int32_t* y = it + 4 * static_cast<size_t>(b);
@@ -114,7 +119,7 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector
     Load& top = heap.back();
     owner[static_cast<size_t>(k)] = top.second;
     ++count[static_cast<size_t>(top.second)];
-    top.first += 4 * static_cast<int64_t>(lut.items[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4 + 3]) + 2;
+    top.first += 4 * static_cast<int64_t>(list[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4 + 3]) + 2;
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
   start.assign(static_cast<size_t>(grid) + 1, 0);
@@ -125,7 +130,7 @@ void bsa::build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector
   for (int k = 0; k < n; ++k) {
     const int32_t pos = fill[static_cast<size_t>(owner[static_cast<size_t>(k)])]++;
     std::memcpy(&items[static_cast<size_t>(pos) * 4],
-                &lut.items[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4], 16);
+                &list[static_cast<size_t>(order[static_cast<size_t>(k)]) * 4], 16);
   }
 }
 
@@ -140,6 +145,36 @@ void bsa::device_records(const bsa_lut& lut, const std::vector<int32_t>& items,
     records[k + 2] = lut.row_ptr[static_cast<size_t>(row)];
     records[k + 3] = nnz | ((lut.diag_pos[static_cast<size_t>(row)] + 1) << 16);
   }
+}
+
+namespace {
+
+// Device records of a regrouped column work list ({b, h, j, count} items):
+// {b*H + h, j, first row_idx entry of the column, count | (dpos + 1) << 16}.
+void csc_records(const bsa_lut& lut, const std::vector<int32_t>& items,
+                 std::vector<int32_t>& records) {
+  records.resize(items.size());
+  for (size_t k = 0; k + 3 < items.size(); k += 4) {
+    const int32_t b = items[k], h = items[k + 1], j = items[k + 2], cnt = items[k + 3];
+    const int32_t col = h * lut.nb + j;
+    records[k] = b * lut.H + h;
+    records[k + 1] = j;
+    records[k + 2] = lut.col_ptr[static_cast<size_t>(col)];
+    records[k + 3] = cnt | ((lut.diag_pos_t[static_cast<size_t>(col)] + 1) << 16);
+  }
+}
+
+}  // namespace
+
+cudaError_t bsa::launch_bwd_variant(int block, int d, bool kv, const BwdParams& p,
+                                    const CUtensorMap& a, const CUtensorMap& b,
+                                    const CUtensorMap& x, const CUtensorMap& y, int grid,
+                                    cudaStream_t stream) {
+  if (block == 128)
+    return d == 128 ? launch_bwd_b128_d128(kv, p, a, b, x, y, grid, stream)
+                    : launch_bwd_b128_d64(kv, p, a, b, x, y, grid, stream);
+  return d == 128 ? launch_bwd_b64_d128(kv, p, a, b, x, y, grid, stream)
+                  : launch_bwd_b64_d64(kv, p, a, b, x, y, grid, stream);
 }
 
 cudaError_t bsa::launch_fwd_variant(int q_block, int kv_block, int d, bool ext,
@@ -175,6 +210,13 @@ bool bsa::schedule_by_head(int policy, int64_t B, int64_t H, int64_t L, int64_t 
 namespace {
 
 void free_device(bsa_lut* lut) {
+  if (lut->d_row_idx) cudaFree(lut->d_row_idx);
+  lut->d_row_idx = nullptr;
+  for (int o = 0; o < 2; ++o) {
+    if (lut->d_items_t[o]) cudaFree(lut->d_items_t[o]);
+    if (lut->d_sched_start_t[o]) cudaFree(lut->d_sched_start_t[o]);
+    lut->d_items_t[o] = lut->d_sched_start_t[o] = nullptr;
+  }
   if (lut->d_col_idx) cudaFree(lut->d_col_idx);
   if (lut->d_items) cudaFree(lut->d_items);
   if (lut->d_status) cudaFree(lut->d_status);
@@ -241,6 +283,44 @@ int bsa_build_lut_rect(const int32_t* layout, int H, int nb, int nbk, int batch,
       const int i = r % nb;
       for (int e = lut->row_ptr[r]; e < lut->row_ptr[r + 1]; ++e)
         if (lut->col_idx[e] == i) lut->diag_pos[r] = e - lut->row_ptr[r];
+    }
+    // Column view for the backward's key-side walk (square layouts).
+    if (nb == nbk) {
+      lut->has_csc = true;
+      lut->col_ptr.assign(rows + 1, 0);
+      for (int h = 0; h < H; ++h)
+        for (int j = 0; j < nb; ++j) {
+          int cnt = 0;
+          for (int i = 0; i < nb; ++i) cnt += layout[(static_cast<int64_t>(h) * nb + i) * nb + j];
+          lut->col_ptr[h * nb + j + 1] = lut->col_ptr[h * nb + j] + cnt;
+        }
+      lut->row_idx.resize(lut->nnz_total);
+      lut->diag_pos_t.assign(rows, -1);
+      for (int h = 0; h < H; ++h)
+        for (int j = 0; j < nb; ++j) {
+          int32_t* dst = lut->row_idx.data() + lut->col_ptr[h * nb + j];
+          int e = 0;
+          for (int i = 0; i < nb; ++i)
+            if (layout[(static_cast<int64_t>(h) * nb + i) * nb + j]) {
+              if (i == j) lut->diag_pos_t[h * nb + j] = e;
+              dst[e++] = i;
+            }
+        }
+      lut->items_t.resize(static_cast<size_t>(n_items) * 4);
+      std::vector<int32_t> rawt(static_cast<size_t>(n_items) * 4);
+      size_t wt = 0;
+      for (int b = 0; b < batch; ++b)
+        for (int h = 0; h < H; ++h)
+          for (int j = 0; j < nb; ++j) {
+            rawt[wt++] = b;
+            rawt[wt++] = h;
+            rawt[wt++] = j;
+            rawt[wt++] = lut->col_ptr[h * nb + j + 1] - lut->col_ptr[h * nb + j];
+          }
+      std::vector<const int32_t*> idt(static_cast<size_t>(n_items));
+      for (size_t e = 0; e < idt.size(); ++e) idt[e] = rawt.data() + 4 * e;
+      std::stable_sort(idt.begin(), idt.end(), less_global);
+      for (size_t e = 0; e < idt.size(); ++e) std::memcpy(&lut->items_t[4 * e], idt[e], 16);
     }
     lut->n_items = static_cast<int>(n_items);
     std::vector<int32_t> raw(static_cast<size_t>(n_items) * 4);
@@ -353,6 +433,39 @@ int bsa_lut_upload(bsa_lut* lut, void* stream) {
                             cudaMemcpyHostToDevice, st) == cudaSuccess &&
             cudaMemsetAsync(lut->d_status, 0, 16, st) == cudaSuccess &&
             cudaStreamSynchronize(st) == cudaSuccess;
+  if (ok && lut->has_csc) {
+    try {
+      for (int o = 0; o < 2; ++o) {
+        std::vector<int32_t> it;
+        bsa::build_schedule_list(lut->items_t, lut->sched_grid, o == 1, it, lut->sched_start_t[o]);
+        csc_records(*lut, it, lut->sched_records_t[o]);
+      }
+    } catch (const std::bad_alloc&) {
+      free_device(lut);
+      return BSA_ERR_ALLOC;
+    }
+    const size_t nr = std::max<size_t>(lut->row_idx.size(), 1) * 4;
+    if (cudaMalloc(&lut->d_row_idx, nr) != cudaSuccess ||
+        cudaMalloc(&lut->d_items_t[0], ni) != cudaSuccess ||
+        cudaMalloc(&lut->d_items_t[1], ni) != cudaSuccess ||
+        cudaMalloc(&lut->d_sched_start_t[0], ns) != cudaSuccess ||
+        cudaMalloc(&lut->d_sched_start_t[1], ns) != cudaSuccess) {
+      free_device(lut);
+      cudaGetLastError();
+      return BSA_ERR_ALLOC;
+    }
+    ok = lut->row_idx.empty() ||
+         cudaMemcpyAsync(lut->d_row_idx, lut->row_idx.data(), lut->row_idx.size() * 4,
+                         cudaMemcpyHostToDevice, st) == cudaSuccess;
+    for (int o = 0; o < 2 && ok; ++o)
+      ok = (lut->sched_records_t[o].empty() ||
+            cudaMemcpyAsync(lut->d_items_t[o], lut->sched_records_t[o].data(),
+                            lut->sched_records_t[o].size() * 4, cudaMemcpyHostToDevice,
+                            st) == cudaSuccess) &&
+           cudaMemcpyAsync(lut->d_sched_start_t[o], lut->sched_start_t[o].data(), ns,
+                           cudaMemcpyHostToDevice, st) == cudaSuccess;
+    ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+  }
   if (!ok) {
     free_device(lut);
     return BSA_ERR_CUDA;
@@ -484,6 +597,76 @@ int bsa_forward_ext(const void* q, const void* k, const void* v, const bsa_lut* 
   const cudaError_t e = bsa::launch_fwd_variant(q_block, kv_block, d, true, p, tq, tk, tv, grid,
                                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+int bsa_lut_export_csc(const bsa_lut* lut, int32_t* col_ptr, int32_t* row_idx, int32_t* items) {
+  if (lut == nullptr) return BSA_ERR_NULL;
+  if (!lut->has_csc) return BSA_ERR_SHAPE;
+  if (col_ptr) std::memcpy(col_ptr, lut->col_ptr.data(), lut->col_ptr.size() * 4);
+  if (row_idx && !lut->row_idx.empty())
+    std::memcpy(row_idx, lut->row_idx.data(), lut->row_idx.size() * 4);
+  if (items) std::memcpy(items, lut->items_t.data(), lut->items_t.size() * 4);
+  return BSA_OK;
+}
+
+int bsa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, const bsa_lut* lut, void* dq, void* dk, void* dv, float* delta,
+                 int B, int H, int L, int d, float scale, int block, int causal_diag,
+                 void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
+      dout == nullptr || lut == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      delta == nullptr)
+    return BSA_ERR_NULL;
+  if ((block != 64 && block != 128) || (d != 64 && d != 128)) return BSA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return BSA_ERR_UNSUPPORTED;
+  if (!lut->has_csc || B != lut->batch || H != lut->H || L <= 0 ||
+      static_cast<int64_t>(lut->nb) * block != L)
+    return BSA_ERR_SHAPE;
+  const int64_t rows = static_cast<int64_t>(B) * H * L;
+  if (rows > kInt32Max - 128) return BSA_ERR_SHAPE;
+  for (const void* ptr : {q, k, v, out, static_cast<const void*>(lse), dout,
+                          static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv), static_cast<const void*>(delta)})
+    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  if (lut->d_items_t[0] == nullptr) return BSA_ERR_STATE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev != lut->device) return BSA_ERR_STATE;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_rows(&tq, q, rows, d, block, d / 64) || !encode_rows(&tk, k, rows, d, block, d / 64) ||
+      !encode_rows(&tv, v, rows, d, block, d / 64) ||
+      !encode_rows(&tdo, dout, rows, d, block, d / 64))
+    return BSA_ERR_CUDA;
+  const int grid = lut->sched_grid;
+  if (grid <= 0) return BSA_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int o = bsa::schedule_by_head(lut->sched_policy, B, H, L, d, dev) ? 1 : 0;
+  bsa::BwdParams p{};
+  p.lse = lse;
+  p.delta = delta;
+  p.status = lut->d_status;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale = scale;
+  p.causal_diag = causal_diag != 0;
+  p.L = L;
+  p.wait_limit_ns = lut->wait_limit_ns;
+  p.expire_site = lut->expire_site;
+  // delta = rowsum(dO * O), then dQ over the rows, then dK and dV over the columns.
+  if (bsa::launch_bwd_delta(out, dout, delta, rows, d, st) != cudaSuccess) return BSA_ERR_CUDA;
+  p.items = reinterpret_cast<const int4*>(o ? lut->d_items_g : lut->d_items);
+  p.cta_start = o ? lut->d_sched_start_g : lut->d_sched_start;
+  p.col_idx = lut->d_col_idx;
+  p.out1 = dq;
+  if (bsa::launch_bwd_variant(block, d, false, p, tq, tdo, tk, tv, grid, st) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  p.items = reinterpret_cast<const int4*>(lut->d_items_t[o]);
+  p.cta_start = lut->d_sched_start_t[o];
+  p.col_idx = lut->d_row_idx;
+  p.out1 = dv;
+  p.out2 = dk;
+  if (bsa::launch_bwd_variant(block, d, true, p, tk, tv, tq, tdo, grid, st) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  return BSA_OK;
 }
 
 int bsa_device_status(const bsa_lut* lut, void* stream, int32_t* detail) {

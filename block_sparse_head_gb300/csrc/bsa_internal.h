@@ -24,6 +24,14 @@ struct bsa_lut {
   std::vector<int32_t> sched_items[2];  // [n_items][4]
   std::vector<int32_t> sched_start[2];  // [sched_grid + 1]
   std::vector<int32_t> sched_records[2];  // device records of sched_items (device_records)
+  // Column view (square layouts only; the backward's key-side walk): col_ptr over
+  // columns h*nb + j, row_idx the active query blocks i ascending, items_t one
+  // {b, h, j, count} per (batch, head, key block) sorted by (-count, b, h, j), diag_pos_t
+  // the position of i == j in each column (-1: none); and its two per-CTA schedules.
+  bool has_csc = false;
+  std::vector<int32_t> col_ptr, row_idx, items_t, diag_pos_t;
+  std::vector<int32_t> sched_records_t[2];
+  std::vector<int32_t> sched_start_t[2];
   // device copies (valid after bsa_lut_upload)
   int device = -1;
   int32_t* d_col_idx = nullptr;
@@ -32,6 +40,9 @@ struct bsa_lut {
   int32_t* d_sched_start = nullptr;  // device copy of sched_start[0] (d_items: records of sched_items[0])
   int32_t* d_items_g = nullptr;        // records of sched_items[1]
   int32_t* d_sched_start_g = nullptr;  // sched_start[1]
+  int32_t* d_row_idx = nullptr;        // column view: row_idx
+  int32_t* d_items_t[2] = {nullptr, nullptr};        // records of both column schedules
+  int32_t* d_sched_start_t[2] = {nullptr, nullptr};
   uint64_t wait_limit_ns = 10000000000ull;
   int expire_site = 0;  // bsa_debug_expire_wait
 };
@@ -78,6 +89,9 @@ enum WaitSite : int {
 // by_head: hand the items out (batch, head) by (batch, head) instead of in list order.
 void build_schedule(const bsa_lut& lut, int grid, bool by_head, std::vector<int32_t>& items,
                     std::vector<int32_t>& start);
+// The same for any work list `list` of {b, h, block, count} items.
+void build_schedule_list(const std::vector<int32_t>& list, int grid, bool by_head,
+                         std::vector<int32_t>& items, std::vector<int32_t>& start);
 
 // Device records of a regrouped work list `items` ({b, h, i, nnz} each):
 // {b*H + h, i, first col_idx entry of the row, nnz | (dpos + 1) << 16} with dpos the
@@ -121,6 +135,45 @@ cudaError_t launch_fwd_q128_k64_d64(bool ext, const FwdParams& p, const CUtensor
 cudaError_t launch_fwd_q128_k64_d128(bool ext, const FwdParams& p, const CUtensorMap& q,
                                     const CUtensorMap& k, const CUtensorMap& v, int grid,
                                     cudaStream_t stream);
+
+// Backward kernel arguments besides the four tensor maps (item tiles A, B; step tiles X, Y).
+struct BwdParams {
+  const int4* items;         // work list regrouped per CTA (records as in the forward)
+  const int32_t* cta_start;  // CTA c takes items[cta_start[c] .. cta_start[c+1])
+  const int32_t* col_idx;    // dQ: key blocks of each row; dK/dV: query blocks of each column
+  const float* lse;          // [B,H,L] from the forward
+  const float* delta;        // [B,H,L] = rowsum(dO * O)
+  void* out1;                // dQ mode: dq; dK/dV mode: dv   (bf16 [B,H,L,d])
+  void* out2;                // dK/dV mode: dk
+  int32_t* status;
+  float scale_log2;          // scale * log2(e)
+  float scale;
+  int causal_diag;
+  int L;
+  unsigned long long wait_limit_ns;
+  int expire_site;
+};
+
+// Backward kernels for (block, head_dim); kv selects the dK/dV walk over the columns
+// (else dQ over the rows).  Each (block, head_dim) pair lives in its own translation unit.
+cudaError_t launch_bwd_variant(int block, int d, bool kv, const BwdParams& p, const CUtensorMap& a,
+                               const CUtensorMap& b, const CUtensorMap& x, const CUtensorMap& y,
+                               int grid, cudaStream_t stream);
+cudaError_t launch_bwd_b64_d64(bool kv, const BwdParams& p, const CUtensorMap& a,
+                               const CUtensorMap& b, const CUtensorMap& x, const CUtensorMap& y,
+                               int grid, cudaStream_t stream);
+cudaError_t launch_bwd_b64_d128(bool kv, const BwdParams& p, const CUtensorMap& a,
+                                const CUtensorMap& b, const CUtensorMap& x, const CUtensorMap& y,
+                                int grid, cudaStream_t stream);
+cudaError_t launch_bwd_b128_d64(bool kv, const BwdParams& p, const CUtensorMap& a,
+                                const CUtensorMap& b, const CUtensorMap& x, const CUtensorMap& y,
+                                int grid, cudaStream_t stream);
+cudaError_t launch_bwd_b128_d128(bool kv, const BwdParams& p, const CUtensorMap& a,
+                                 const CUtensorMap& b, const CUtensorMap& x, const CUtensorMap& y,
+                                 int grid, cudaStream_t stream);
+// delta[r] = sum_x dout[r,x] out[r,x] over `rows` rows of d bf16 (fp32 result).
+cudaError_t launch_bwd_delta(const void* out, const void* dout, float* delta, int64_t rows, int d,
+                             cudaStream_t stream);
 
 // One-CTA kernel whose only wait never completes; it must give up after limit_ns.
 cudaError_t launch_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);

@@ -225,6 +225,45 @@ int bsa_forward_ext(const void* q, const void* k, const void* v, const bsa_lut* 
                     int kv_block, int causal_diag, const bsa_ext_args* ext, void* stream);
 
 /*
+ * bsa_lut_export_csc -- the column view the backward walks (square layouts only):
+ * col_ptr int32[H*nb + 1] over columns h*nb + j, row_idx int32[nnz] with the active query
+ * blocks i of each column ascending, items int32[B*H*nb][4] = {b, h, j, count}, sorted
+ * stably by (-count, b, h, j).  Any pointer may be NULL.  Errors: BSA_ERR_NULL,
+ * BSA_ERR_SHAPE (rectangular layout).
+ */
+int bsa_lut_export_csc(const bsa_lut* lut, int32_t* col_ptr, int32_t* row_idx, int32_t* items);
+
+/*
+ * bsa_backward -- gradients of the forward (the operation above) with respect to q, k
+ * and v, given the forward's out and lse and the upstream gradient dout.  Gradients flow
+ * through the active blocks only ("Block Sparse Attention Techniques", section 2,
+ * "Gradient Propagation in Block Sparse Attention"); with P the masked softmax:
+ *
+ *   delta[r] = sum_x dout[r,x] out[r,x]
+ *   dS = P * (dout V^T - delta),   dq = scale dS K,   dk = scale dS^T Q,   dv = P^T dout
+ *
+ * P is recomputed from q, k and lse (P = exp(scale q.k - lse) on the active entries).
+ *
+ *   q, k, v, out, dout   device bf16 [B,H,L,d] (out, lse: the bsa_forward results for
+ *                        these q, k, v and arguments).
+ *   lse                  device fp32 [B,H,L].
+ *   lut                  uploaded LUT of a square layout (bsa_build_lut).
+ *   dq, dk, dv           device bf16 [B,H,L,d]; every element written (rows and keys with
+ *                        no active entry get 0).
+ *   delta                device fp32 [B,H,L], caller-owned workspace; overwritten.
+ *   B .. causal_diag     as bsa_forward.
+ *
+ * All pointers 16-byte aligned.  Asynchronous: queues three kernels on `stream` (delta,
+ * then dq over the layout's rows, then dk and dv over its columns); allocates nothing.
+ * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_ALIGN, BSA_ERR_UNSUPPORTED, BSA_ERR_STATE,
+ * BSA_ERR_CUDA.  Device timeouts are reported by bsa_device_status as for the forward.
+ */
+int bsa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, const bsa_lut* lut, void* dq, void* dk, void* dv, float* delta,
+                 int B, int H, int L, int d, float scale, int block, int causal_diag,
+                 void* stream);
+
+/*
  * bsa_forward_noalloc -- the same forward as bsa_forward for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call.
  *

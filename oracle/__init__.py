@@ -5,6 +5,7 @@ from .bsa_oracle import (  # noqa: F401
     ORDER_GROUPED,
     active_keys,
     backward,
+    backward_blocks,
     block_flops,
     check_layout,
     expand_mask,

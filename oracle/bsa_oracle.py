@@ -304,6 +304,43 @@ def backward(q, k, v, do, layout, scale: float, block: int, causal_diag: bool):
     return dq, dk, dv
 
 
+def backward_blocks(q, k, v, do, layout, scale: float, block: int, causal_diag: bool):
+    """``backward`` computed query block by query block over the active keys only.
+
+    Entries outside the active blocks have P = 0 and contribute nothing to any of the
+    three gradients, so leaving them out changes nothing (pinned against ``backward``).
+    For each query block the same formulas run on the gathered active keys; dK and dV
+    rows collect the contributions of every query block that attends them."""
+    lay = check_layout(layout)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, L, d = q.shape
+    nb = lay.shape[1]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nb):
+                active = [j for j in range(nb) if lay[h, i, j] == 1]
+                if not active:
+                    continue
+                rows = np.arange(i * block, (i + 1) * block)
+                cols = np.concatenate([np.arange(j * block, (j + 1) * block) for j in active])
+                mask = np.ones((block, cols.size), dtype=bool)
+                if causal_diag:
+                    mask &= ~((cols[None, :] // block == i) & (cols[None, :] > rows[:, None]))
+                s = np.where(mask, scale * (q[b, h, rows] @ k[b, h, cols].T), -np.inf)
+                e = np.exp(s - s.max(axis=1, keepdims=True))
+                p = e / e.sum(axis=1, keepdims=True)
+                dp = do[b, h, rows] @ v[b, h, cols].T
+                ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+                dq[b, h, rows] = scale * (ds @ k[b, h, cols])
+                dk[b, h, cols] += scale * (ds.T @ q[b, h, rows])
+                dv[b, h, cols] += p.T @ do[b, h, rows]
+    return dq, dk, dv
+
+
 def oracle_csc(layout, batch: int):
     """Column view of the layout for the key-side gradients: for each (h, j) the active
     query blocks i ascending (col_ptr [H*nb+1], row_idx [nnz]) and one item

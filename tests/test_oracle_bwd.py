@@ -178,3 +178,17 @@ def test_pins_catch_planted_mistakes(mutant):
         except Exception:
             errs.append(math.inf)
     assert max(errs) > 1e-6
+
+
+def test_block_restricted_equals_dense():
+    """Skipping the entries outside the active blocks changes no gradient."""
+    for seed, causal, blk in [(41, True, 4), (42, False, 3), (43, True, 5)]:
+        B, H, nb, d = 2, 3, 5, 6
+        L = nb * blk
+        q, k, v, do = (_rand((B, H, L, d), seed * 10 + s) for s in range(4))
+        lay = wls.random_layout(H, nb, 0.4, seed, empty_rows=1).numpy()
+        lay[:, np.arange(nb), np.arange(nb)] = 1
+        lay[1, 2] = 0
+        a = oracle.backward(q, k, v, do, lay, 0.4, blk, causal)
+        b = oracle.backward_blocks(q, k, v, do, lay, 0.4, blk, causal)
+        assert _err(a, b) < 1e-12
