@@ -11,7 +11,8 @@ Under torchrun every rank runs its own replica of the workload (weak scaling) an
 slowest rank's time counts.
 
 After the headline the forward is timed alone, by the same method, on the other
-workloads of the 55% target (3 and 4 by default), reported under ``per_workload``.
+workloads of the 55% target (3 and 4 by default), reported under ``per_workload``, and
+the backward (dQ, dK, dV) on workloads 3, 4 and 5 under ``backward``.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the same
 workload (query blocks drawn across the work list), one process per host core.
@@ -280,11 +281,13 @@ def workload_config(wl, l2_note: str, world: int) -> dict:
 
 
 def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds: float,
-                max_steps: int, gpu: int) -> dict:
-    """Device time of the forward alone on workload `index` (no e2e leg): CUDA events
-    around each launch on the launching stream, the L2 flushed between launches when the
-    inputs would fit in it, clocks sampled during the timed region, which lasts at least
-    `min_seconds` (and at least `min_steps` launches)."""
+                max_steps: int, gpu: int, backward: bool = False) -> dict:
+    """Device time of the forward alone on workload `index` (no e2e leg), or of the
+    backward (three kernels: delta, dQ, dK/dV): CUDA events around each step on the
+    launching stream, the L2 flushed between steps when the inputs would fit in it,
+    clocks sampled during the timed region, which lasts at least `min_seconds` (and at
+    least `min_steps` steps).  The backward counts 10 * block^2 * d FLOPs per active
+    block per batch entry (2.5 times the forward: dS, dQ, dK, dV and the recomputed S)."""
     import torch
 
     import block_sparse_head_gb300 as bsa
@@ -292,7 +295,7 @@ def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds
 
     wl = wls.WORKLOADS[index]
     lay = wls.layout_for(wl)
-    flops_step = 4 * wl.block * wl.block * wl.d * int(lay.sum()) * wl.B
+    flops_step = (10 if backward else 4) * wl.block * wl.block * wl.d * int(lay.sum()) * wl.B
     q, k, v = wls.qkv(wl)
     lut = bsa.build_lut(lay, wl.B, order)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
@@ -302,13 +305,24 @@ def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds
     stream = torch.cuda.current_stream()
     flush = None
     l2_note = "inputs larger than L2"
-    if 3 * qd.numel() * 2 < 2 * L2_BYTES:
+    if (5 if backward else 3) * qd.numel() * 2 < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
         l2_note = "L2 flushed between steps (256 MiB write, outside the events)"
 
-    def step():
+    if backward:
         bsa.forward(qd, kd, vd, lut, wl.scale, wl.block, wl.causal_diag, out=out, lse=lse,
                     stream=stream)
+        dout = wls.randn_qkv(wl.B, wl.H, wl.L, wl.d, seed=5000 + index)[0].cuda()
+        grads = tuple(torch.empty_like(qd) for _ in range(3))
+        delta = torch.empty_like(lse)
+
+        def step():
+            bsa.backward(qd, kd, vd, out, lse, dout, lut, wl.scale, wl.block, wl.causal_diag,
+                         *grads, delta=delta, stream=stream)
+    else:
+        def step():
+            bsa.forward(qd, kd, vd, lut, wl.scale, wl.block, wl.causal_diag, out=out, lse=lse,
+                        stream=stream)
 
     for _ in range(warmup):
         step()
@@ -352,7 +366,7 @@ def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds
                          "frac": round(achieved / peaks[peak_kind], 4),
                          "peak_source": f"{peaks['source']} {peak_kind} (MEASURED_PEAKS.json)",
                          "traffic": recorded_traffic(wl.name), "flops_per_launch": flops_step},
-            "gpu_launches": n, "clocks": clk}
+            "gpu_launches": n * (3 if backward else 1), "clocks": clk}
 
 
 def gpu_arm(args) -> None:
@@ -528,6 +542,15 @@ def gpu_arm(args) -> None:
                             20000, local)
             line["per_workload"][wls.WORKLOADS[index].name] = r
             torch.cuda.empty_cache()
+    bwd = [int(x) for x in args.backward_workloads.split(",") if x.strip()] if world == 1 else []
+    if bwd:
+        # The backward (bsa_backward: delta, dQ, dK/dV kernels) on the same workloads.
+        line["backward"] = {}
+        for index in bwd:
+            r = time_kernel(index, args.order, max(3, args.warmup), 10, args.min_seconds, 5000,
+                            local, backward=True)
+            line["backward"][wls.WORKLOADS[index].name] = r
+            torch.cuda.empty_cache()
     if not args.no_cpu_baseline and world == 1:
         cb = cpu_baseline(wl, q, k, v, lay, args.cpu_budget)
         line["cpu_baseline"] = {
@@ -603,6 +626,8 @@ def main() -> None:
                     help="query blocks per host core in each reference step")
     ap.add_argument("--extra-workloads", default="3,4",
                     help="other workloads timed (kernel only) after the headline, comma list")
+    ap.add_argument("--backward-workloads", default="3,4,5",
+                    help="workloads whose backward is timed after the forward, comma list")
     ap.add_argument("--min-seconds", type=float, default=0.5,
                     help="shortest timed region of each extra workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")

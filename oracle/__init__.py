@@ -17,3 +17,4 @@ from .bsa_oracle import (  # noqa: F401
     query_block,
 )
 from .bsa_oracle_ext import element_mask, forward_ext, n_blocks  # noqa: F401,E402
+from .bsa_oracle_topk import topk_attention, topk_flops  # noqa: F401,E402
