@@ -12,7 +12,8 @@ slowest rank's time counts.
 
 After the headline the forward is timed alone, by the same method, on the other
 workloads of the 55% target (3 and 4 by default), reported under ``per_workload``, and
-the backward (dQ, dK, dV) on workloads 3, 4 and 5 under ``backward``.
+the backward (dQ, dK, dV) on workloads 3, 4 and 5 under ``backward``, and the top-k
+token-gather attention workload under ``topk``.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the same
 workload (query blocks drawn across the work list), one process per host core.
@@ -369,6 +370,70 @@ def time_kernel(index: int, order: str, warmup: int, min_steps: int, min_seconds
             "gpu_launches": n * (3 if backward else 1), "clocks": clk}
 
 
+def time_topk(warmup: int, min_steps: int, min_seconds: float, max_steps: int, gpu: int) -> dict:
+    """Device time of bsa_topk_forward on the top-k workload (64 heads of 512, 4096
+    positions listing 2048 rows each of a 65536-row context), by the forward's method;
+    4 * H * D FLOPs per valid listed row."""
+    import torch
+
+    import block_sparse_head_gb300 as bsa
+    from block_sparse_head_gb300 import workloads as wls
+
+    wl = wls.TOPK
+    q, kv, sink, idx = (t.cuda() for t in wls.topk_inputs(wl.B, wl.M, wl.N, wl.H, wl.D, wl.K,
+                                                           seed=2024))
+    flops_step = 4 * wl.H * wl.D * int(((idx >= 0) & (idx < wl.N)).sum())
+    out = torch.empty_like(q)
+    lse = torch.empty(wl.B, wl.M, wl.H, device="cuda", dtype=torch.float32)
+    status = torch.zeros(4, device="cuda", dtype=torch.int32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        bsa.topk_forward(q, kv, sink, idx, wl.scale, out=out, lse=lse, status=status,
+                         stream=stream)
+
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(3):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = e0.elapsed_time(e1) / 3
+    if int(status[0]) != 0:
+        raise RuntimeError(f"top-k status {int(status[0]):#x} during warm-up")
+    n = int(min(max_steps, max(min_steps, math.ceil(min_seconds * 1e3 / max(est_ms, 1e-3)))))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    clocks = ClockSampler(gpu)
+    time.sleep(0.3)
+    for i in range(n):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(status[0]) != 0:
+        raise RuntimeError(f"top-k status {int(status[0]):#x} in the timed region")
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(per_ms)
+    peaks = measured_peaks()
+    peak_kind = "bf16_burst" if total_ms < 3000 else "bf16_sustained"
+    achieved = flops_step / (statistics.mean(per_ms) * 1e-3) / 1e12
+    return {"config": {"workload": f"{wl.name} (top-k token gather with sink)", "batch": wl.B,
+                       "positions": wl.M, "kv_rows": wl.N, "heads": wl.H, "head_dim": wl.D,
+                       "topk": wl.K, "l2": "inputs larger than L2"},
+            "steps": n, "ms_per_step": round(total_ms / n, 5), "value": round(achieved, 2),
+            "unit": "TFLOPS", "pct_of_peak": round(100 * achieved / peaks[peak_kind], 2),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks[peak_kind], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks[peak_kind], 4),
+                         "peak_source": f"{peaks['source']} {peak_kind} (MEASURED_PEAKS.json)",
+                         "traffic": None, "flops_per_launch": flops_step},
+            "gpu_launches": n, "clocks": clk}
+
+
 def gpu_arm(args) -> None:
     import numpy as np  # noqa: F401
     import torch
@@ -551,6 +616,10 @@ def gpu_arm(args) -> None:
                             local, backward=True)
             line["backward"][wls.WORKLOADS[index].name] = r
             torch.cuda.empty_cache()
+    if args.topk and world == 1:
+        # The second workload: top-k token-gather attention with a sink.
+        line["topk"] = time_topk(max(3, args.warmup), 10, args.min_seconds, 5000, local)
+        torch.cuda.empty_cache()
     if not args.no_cpu_baseline and world == 1:
         cb = cpu_baseline(wl, q, k, v, lay, args.cpu_budget)
         line["cpu_baseline"] = {
@@ -628,6 +697,8 @@ def main() -> None:
                     help="other workloads timed (kernel only) after the headline, comma list")
     ap.add_argument("--backward-workloads", default="3,4,5",
                     help="workloads whose backward is timed after the forward, comma list")
+    ap.add_argument("--no-topk", dest="topk", action="store_false",
+                    help="skip the top-k token-gather workload")
     ap.add_argument("--min-seconds", type=float, default=0.5,
                     help="shortest timed region of each extra workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")

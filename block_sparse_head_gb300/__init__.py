@@ -15,4 +15,5 @@ from .binding import (  # noqa: F401
     forward_ext,
     library_path,
     load_library,
+    topk_forward,
 )

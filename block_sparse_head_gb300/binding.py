@@ -31,7 +31,7 @@ EXPORTED = (
     "bsa_wait_selftest",
     "bsa_status_string", "bsa_version", "bsa_forward_noalloc", "bsa_debug_expire_wait",
     "bsa_build_lut_rect", "bsa_lut_kv_blocks", "bsa_forward_ext", "bsa_lut_export_csc",
-    "bsa_backward",
+    "bsa_backward", "bsa_topk_forward",
 )
 
 
@@ -80,6 +80,9 @@ def load_library():
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(ExtArgs), vp]
+        lib.bsa_topk_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_float, vp]
         lib.bsa_lut_export_csc.argtypes = [vp, vp, vp, vp]
         lib.bsa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
@@ -111,7 +114,7 @@ def load_library():
                      "bsa_forward", "bsa_device_status", "bsa_set_schedule", "bsa_set_wait_limit",
                      "bsa_wait_selftest", "bsa_debug_expire_wait", "bsa_build_lut_rect",
                      "bsa_lut_kv_blocks", "bsa_forward_ext", "bsa_lut_export_csc",
-                     "bsa_backward"):
+                     "bsa_backward", "bsa_topk_forward"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -324,6 +327,33 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
                             float(scale), int(block), int(bool(causal_diag)),
                             _stream_handle(stream)), "bsa_backward")
     return dq, dk, dv
+
+
+def topk_forward(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torch.Tensor,
+                 scale: float, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 status: torch.Tensor | None = None, stream=None):
+    """Top-k token-gather attention with a sink (bsa_topk_forward).  q bf16 [B, M, H, D],
+    kv bf16 [B, N, D], sink fp32 [H], idx int32 [B, M, K] (-1: unused).  Returns
+    (out bf16 [B, M, H, D], lse fp32 [B, M, H], status int32 [1]); a nonzero status
+    (read after the stream is synchronized) means a bounded wait gave up."""
+    lib = load_library()
+    B, M, H, D = q.shape
+    N, K = kv.shape[1], idx.shape[2]
+    _check_qkv(q, "q", (B, M, H, D))
+    _check_qkv(kv, "kv", (B, N, D))
+    if not sink.is_cuda or sink.dtype != torch.float32 or tuple(sink.shape) != (H,):
+        raise ValueError("sink must be a CUDA fp32 tensor of shape [H]")
+    if not idx.is_cuda or idx.dtype != torch.int32 or not idx.is_contiguous() or idx.shape[:2] != (B, M):
+        raise ValueError("idx must be a contiguous CUDA int32 tensor [B, M, K]")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, M, H, device=q.device, dtype=torch.float32) if lse is None else lse
+    status = torch.zeros(4, device=q.device, dtype=torch.int32) if status is None else status
+    _check_qkv(out, "out", (B, M, H, D))
+    _check(lib.bsa_topk_forward(q.data_ptr(), kv.data_ptr(), sink.contiguous().data_ptr(),
+                                idx.data_ptr(), out.data_ptr(), lse.data_ptr(), status.data_ptr(),
+                                B, M, N, H, D, K, float(scale), _stream_handle(stream)),
+           "bsa_topk_forward")
+    return out, lse, status
 
 
 def forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lut: Lut, scale: float,

@@ -23,9 +23,11 @@ SOURCES = [
     "bsa_host.cpp",
     "bsa_selftest.cu",
     "bsa_noalloc.cu",
+    "bsa_topk.cu",
 ] + [f"bsa_fwd_q{qb}_k{kb}_d{d}.cu" for qb, kb in ((64, 64), (128, 128), (64, 128), (128, 64))
      for d in (64, 128)] + [f"bsa_bwd_b{b}_d{d}.cu" for b in (64, 128) for d in (64, 128)]
-HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_fwd_kernel.cuh", "bsa_bwd_kernel.cuh"]
+HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_fwd_kernel.cuh", "bsa_bwd_kernel.cuh",
+           "bsa_topk_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

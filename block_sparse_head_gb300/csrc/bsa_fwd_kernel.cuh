@@ -120,19 +120,6 @@ struct FwdCfg {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(QB, D, false, true);
 };
 
-// Bounded wait that ignores the abort flag and never records a status: used only
-// to drain work already in flight before the CTA releases its resources.  Its limit
-// is fixed and independent of the (possibly tiny) per-wait limit of the main loop.
-constexpr uint64_t kDrainLimitNs = 4000000000ull;
-
-__device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity,
-                                                uint64_t limit_ns = kDrainLimitNs) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return;
-  }
-}
-
 // Blocks in step s of a row with nnz active blocks.
 template <int G>
 __device__ __forceinline__ int step_blocks(int nnz, int s) {

@@ -149,3 +149,50 @@ def randn_qkv(B: int, H: int, L: int, d: int, seed: int, dtype=torch.bfloat16):
     """Q, K, V ~ N(0, 1) of an arbitrary shape (tests)."""
     g = torch.Generator().manual_seed(seed)
     return tuple(torch.randn(B, H, L, d, generator=g).to(dtype) for _ in range(3))
+
+
+# ------------------------------------------------------- top-k token-gather workload
+
+
+@dataclasses.dataclass(frozen=True)
+class TopkWorkload:
+    """Top-k token-gather attention (the DeepSeek-V4.1 sparse_attn shape: 64 heads of
+    512, one key-value row shared by all heads): M query positions at the end of an
+    N-row context, each listing K rows."""
+    name: str
+    B: int
+    M: int
+    N: int
+    H: int
+    D: int
+    K: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+TOPK = TopkWorkload("topk2048-ctx65536", 1, 4096, 65536, 64, 512, 2048)
+
+
+def topk_inputs(B: int, M: int, N: int, H: int, D: int, K: int, seed: int):
+    """q [B, M, H, D], kv [B, N, D] ~ N(0, 1) rounded to bf16; sink [H] ~ N(0, 1) fp32;
+    idx int32 [B, M, K].
+
+    Position m stands at N - M + m and may list rows 0 .. N - M + m (causal).  Its K
+    rows are drawn one per stratum of that range (row floor((j + u_j) * count / K) for
+    j < K, u_j uniform in [0, 1)), so they are distinct, ascending and spread over the
+    whole context; a position with fewer than K candidates lists them all and pads with -1.
+    """
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, M, H, D, generator=g).to(torch.bfloat16)
+    kv = torch.randn(B, N, D, generator=g).to(torch.bfloat16)
+    sink = torch.randn(H, generator=g)
+    count = (N - M + torch.arange(M) + 1).clamp(min=1)           # candidates per position
+    u = torch.rand(B, M, K, generator=g, dtype=torch.float64)
+    j = torch.arange(K, dtype=torch.float64)
+    idx = torch.floor((j + u) * count[None, :, None].double() / K).to(torch.int64)
+    short = count[None, :, None] < K                                 # fewer candidates than K
+    idx = torch.where(short, torch.where(j[None, None, :] < count[None, :, None],
+                                         j.to(torch.int64)[None, None, :].expand(B, M, K), -1), idx)
+    return q, kv, sink, idx.to(torch.int32)

@@ -264,6 +264,37 @@ int bsa_backward(const void* q, const void* k, const void* v, const void* out, c
                  void* stream);
 
 /*
+ * bsa_topk_forward -- top-k token-gather attention with an attention sink, the second
+ * sparsity granularity of the pages: the sparse_attn kernel of the DeepSeek-V4.1
+ * "Sparse attention / Weighted row sum" page.  Every query position lists K rows of its
+ * batch's key-value matrix; a row is both key and value and is shared by all H heads;
+ * each head's sink logit adds one term to the softmax denominator.  For batch b,
+ * position m, head h, with J the list entries whose index lies in [0, N) (-1 marks an
+ * unused slot; any other index outside [0, N) is treated the same; a row listed twice
+ * counts twice):
+ *
+ *   s_j = scale * <q[b,m,h,:], kv[b, idx[b,m,j], :]>
+ *   Z   = sum_{j in J} exp(s_j) + exp(sink[h])
+ *   out[b,m,h,:] = sum_{j in J} exp(s_j) / Z * kv[b, idx[b,m,j], :],   lse[b,m,h] = ln Z
+ *
+ * (a position with no valid entry gets out = 0 and lse = sink[h], the page's all-zero
+ * convention).
+ *
+ *   q       device bf16 [B, M, H, D];  kv  device bf16 [B, N, D];  out  bf16 [B, M, H, D].
+ *   sink    device fp32 [H];  idx  device int32 [B, M, K];  lse  device fp32 [B, M, H].
+ *   status  device int32, caller-owned, zero before the call: a bounded wait that gives
+ *           up in the kernel writes 0x10000 | site there (and the outputs are undefined).
+ *   H must be 64 and D 512 (the page's shape); K >= 1 (the list runs in steps of 128).
+ *
+ * All pointers 16-byte aligned (status 4-byte).  Asynchronous, one kernel launch,
+ * allocates nothing.  Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_ALIGN,
+ * BSA_ERR_UNSUPPORTED (H, D, or non-finite scale), BSA_ERR_CUDA.
+ */
+int bsa_topk_forward(const void* q, const void* kv, const float* sink, const int32_t* idx,
+                     void* out, float* lse, int32_t* status, int B, int M, int N, int H, int D,
+                     int K, float scale, void* stream);
+
+/*
  * bsa_forward_noalloc -- the same forward as bsa_forward for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call.
  *
