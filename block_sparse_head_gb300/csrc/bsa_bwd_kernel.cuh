@@ -255,7 +255,8 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
 // ----------------------------------------------------------- elementwise warps
 
 template <int BLK, int D, bool KV>
-__device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+__device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sbase,
+                                                const uint8_t* smem, uint32_t tmem,
                                                 const WaitCtl& ctl) {
   using C = BwdCfg<BLK, D, KV>;
   constexpr int G = C::kG;
@@ -268,8 +269,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
   const int row = (BLK == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
   const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (BLK == 128 ? wg * 16 : 0)) << 16);
   const int kbase = (BLK == 128) ? 64 * half : 0;  // first column of this half in its block
-  const float* vec = reinterpret_cast<const float*>(
-      __cvta_shared_to_generic(sbase + C::kOffVec));  // KV: [stage][lse | delta][128]
+  const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec);  // KV: [stage][lse | delta][128]
 
   auto warp_arrive = [&](int b) {
     tc_fence_before();
@@ -374,8 +374,9 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
                    const BwdParams p) {
   using C = BwdCfg<BLK, D, KV>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, by pointer arithmetic on the shared array itself, so that the
+  // compiler keeps shared-memory loads for it.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) bwd_mma<BLK, D, KV>(p, sbase, tmem, ctl);
   } else {
-    bwd_elementwise<BLK, D, KV>(p, sbase, tmem, ctl);
+    bwd_elementwise<BLK, D, KV>(p, sbase, smem, tmem, ctl);
   }
   tc_fence_before();
   __syncthreads();

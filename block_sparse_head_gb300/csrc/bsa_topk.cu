@@ -45,9 +45,9 @@ extern "C" int bsa_topk_forward(const void* q, const void* kv, const float* sink
     return BSA_ERR_ALIGN;
   auto fn = topk_encode_fn();
   if (fn == nullptr) return BSA_ERR_CUDA;
-  // Q as [64 columns, B*M*H rows, D/64 chunks] (box: one position's 64 heads, all
-  // chunks); kv as [D columns, B*N rows] gathered four rows at a time, 64 columns each.
-  CUtensorMap tq, tkv;
+  // Q as [64 columns, B*M*H rows, D/64 chunks]: one box is one position's 64 heads, all
+  // chunks.  (The listed kv rows are gathered by the kernel's own copies.)
+  CUtensorMap tq;
   {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(npos * H), static_cast<cuuint64_t>(D / 64)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, 128};
@@ -58,21 +58,12 @@ extern "C" int bsa_topk_forward(const void* q, const void* kv, const float* sink
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return BSA_ERR_CUDA;
   }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(B) * N};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return BSA_ERR_CUDA;
-  }
   int dev = -1, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return BSA_ERR_CUDA;
   bsa::TopkParams p{};
+  p.kv = kv;
   p.idx = idx;
   p.sink = sink;
   p.out = out;
@@ -94,6 +85,6 @@ extern "C" int bsa_topk_forward(const void* q, const void* kv, const float* sink
   }
   const int grid = static_cast<int>(npos < sms ? npos : sms);
   bsa::bsa_topk_kernel<<<grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(
-      tq, tkv, p);
+      tq, p);
   return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

@@ -17,14 +17,17 @@
 // lanes (a shuffle reduce-scatter within each warp, then shared memory across the four
 // warps).  P^T goes to shared memory as bf16, the B operand of the second product.
 // One CTA per SM walks positions m = blockIdx.x, blockIdx.x + gridDim.x, ...:
-//   warp 0      producer: the position's Q (one 3-D TMA copy, 64 KB) and, per step, the
-//               128 listed rows as eight 64-column chunks by TMA gather4 (four rows per
-//               copy; each lane of the warp gathers four rows).  The gathered tile is
-//               refilled quarter by quarter (128 columns of D) as soon as the previous
-//               step's O^T piece that reads the quarter completed.
+//   warp 0      producer: the position's Q (one 3-D TMA copy, 64 KB).
 //   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2-5   softmax, one per TMEM lane quadrant (row 32*(warp % 4) + lane of the
 //               step), then the epilogue: O^T / l per head, bf16 out[m, h, :] and lse.
+//               They also gather the next step's 128 listed rows (16-byte cp.async
+//               copies into the 128-byte-swizzled operand layout, each warp instruction
+//               reading 512 contiguous bytes) while the tensor core runs this step's
+//               O^T product: the tile is refilled quarter by quarter (128 columns of D)
+//               as soon as the product's piece that reads the quarter completed.  (TMA
+//               gather4 moves four 128-byte row pieces per copy; 256 of them per step
+//               kept the tensor core waiting.)
 // Every wait is bounded (WaitCtl), as in the other kernels.
 #pragma once
 
@@ -65,6 +68,7 @@ struct TopkCfg {
 };
 
 struct TopkParams {
+  const void* kv;       // bf16 [B][N][D]
   const int32_t* idx;   // [B*M][K]
   const float* sink;    // [H]
   void* out;            // bf16 [B*M][H][D]
@@ -79,65 +83,18 @@ struct TopkParams {
 // ------------------------------------------------------------------ producer (warp 0)
 
 __device__ __forceinline__ void topk_producer(const TopkParams& p, const CUtensorMap* tm_q,
-                                              const CUtensorMap* tm_kv, uint32_t sbase,
-                                              const WaitCtl& ctl) {
+                                              uint32_t sbase, const WaitCtl& ctl) {
   using C = TopkCfg;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  const int lane = threadIdx.x & 31;
-  const int nsteps = (p.K + C::kRows - 1) / C::kRows;
-  // All lanes wait (the result is made warp-uniform); lane 0 arms the barriers.
-  auto wait = [&](int b, int parity, int site) {
-    bool w = mbar_wait(bar(b), parity, ctl, site);
-    return __all_sync(0xffffffffu, w);
-  };
-  int item = 0, t = 0;
-  bool ok = true;
-  for (int pos = blockIdx.x; ok && pos < p.npos; pos += gridDim.x, ++item) {
-    const int bi = pos / p.M;
+  int item = 0;
+  for (int pos = blockIdx.x; pos < p.npos; pos += gridDim.x, ++item) {
     // Q: one buffer, free once the previous position's last S^T completed.
-    if (item > 0 && !wait(C::kBarQE, (item - 1) & 1, kSiteProdKEmpty)) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::kBarQF), C::kQBytes);
-      tma_load_3d(sbase + C::kOffQ, tm_q, bar(C::kBarQF), 0, pos * C::kH, 0);
-    }
-    const int32_t* list = p.idx + static_cast<size_t>(pos) * p.K;
-    for (int s = 0; s < nsteps; ++s, ++t) {
-      // This lane gathers rows 4*lane .. 4*lane + 3 of the step; unused or invalid
-      // slots fetch row 0 (their scores are masked by the softmax).
-      int rows[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = s * C::kRows + 4 * lane + i;
-        const int v = (j < p.K) ? list[j] : -1;
-        rows[i] = bi * p.N + ((v >= 0 && v < p.N) ? v : 0);
-      }
-#pragma unroll 1
-      for (int qq = 0; qq < 4; ++qq) {
-        // Quarter qq (chunks 2qq, 2qq+1) held step t-1's rows, read by its O^T piece qq.
-        if (t > 0 && !wait(C::kBarKE + qq, (t - 1) & 1, kSiteProdVEmpty)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(bar(C::kBarKF + qq), 2 * C::kChunkKV);
-        __syncwarp();
-#pragma unroll
-        for (int c = 2 * qq; c < 2 * qq + 2; ++c)
-          tma_gather4(sbase + C::kOffKV + c * C::kChunkKV + lane * 512, tm_kv, bar(C::kBarKF + qq),
-                      64 * c, rows[0], rows[1], rows[2], rows[3]);
-      }
-      if (!ok) {
-        ++t;  // the current step's armed quarters are drained below
-        break;
-      }
-    }
+    if (item > 0 && !mbar_wait(bar(C::kBarQE), (item - 1) & 1, ctl, kSiteProdKEmpty)) break;
+    mbar_arrive_expect_tx(bar(C::kBarQF), C::kQBytes);
+    tma_load_3d(sbase + C::kOffQ, tm_q, bar(C::kBarQF), 0, pos * C::kH, 0);
   }
-  // Wait for every copy issued (immediate on the normal path).
-  if (lane == 0) {
-    if (t > 0)
-      for (int qq = 0; qq < 4; ++qq) mbar_drain_wait(bar(C::kBarKF + qq), (t - 1) & 1, 100000000ull);
-    if (item > 0) mbar_drain_wait(bar(C::kBarQF), (item - 1) & 1, 100000000ull);
-  }
-  __syncwarp();
+  // Wait for the last copy issued (immediate on the normal path).
+  if (item > 0) mbar_drain_wait(bar(C::kBarQF), (item - 1) & 1, 100000000ull);
 }
 
 // ----------------------------------------------------------------- MMA issuer (warp 1)
@@ -264,16 +221,71 @@ __device__ __forceinline__ void topk_softmax(const TopkParams& p, uint32_t sbase
     bool w = mbar_wait(bar(b), parity, ctl, kSiteSoftSFull);
     return __all_sync(0xffffffffu, w);
   };
+  // Gathers step s of position pos (the CTA's step t) into the tile: thread u of the 128
+  // copies, for each quarter qq (columns 128qq .. 128qq + 127 of D), 16 bytes (column piece
+  // jj = 16qq + u % 16) of rows u / 16 + 8k, k < 16 -- two rows of 256 contiguous bytes per
+  // warp instruction -- into the swizzled chunk 2qq + jj / 8.  A quarter is refilled once
+  // the previous step's O^T piece that reads it completed; each warp arrives on the
+  // quarter's barrier when its copies landed.  Unused or invalid slots copy row 0 (finite
+  // data; their scores are masked).
+  const int u = 32 * ((warp - 2) & 3) + lane;
+  auto gather = [&](int gpos, int gs, int gt) -> bool {
+    const int32_t* gl = p.idx + static_cast<size_t>(gpos) * p.K;
+    const int bi = gpos / p.M;
+    const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(p.kv) + static_cast<size_t>(bi) * p.N * C::kD;
+    const int jj = u & 15;
+    const __nv_bfloat16* src[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int j = gs * C::kRows + (u >> 4) + 8 * k;
+      const int v = (j < p.K) ? gl[j] : -1;
+      src[k] = base + static_cast<size_t>((v >= 0 && v < p.N) ? v : 0) * C::kD + 8 * jj;
+    }
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      if (gt > 0 && !wait(C::kBarKE + qq, (gt - 1) & 1, kSiteProdVEmpty)) {
+        cp_async_wait<0>();  // nothing of this thread's may still be landing on exit
+        return false;
+      }
+      const uint32_t chunk = sbase + C::kOffKV + (2 * qq + (jj >> 3)) * C::kChunkKV;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = (u >> 4) + 8 * k;
+        cp_async16(chunk + r * 128 + (((jj & 7) ^ (r & 7)) << 4), src[k] + 128 * qq);
+      }
+      cp_async_commit();
+    }
+    // Quarter qq is complete when at most 3 - qq later groups are still in flight.
+    auto land = [&](int qq) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarKF + qq));
+    };
+    cp_async_wait<3>();
+    land(0);
+    cp_async_wait<2>();
+    land(1);
+    cp_async_wait<1>();
+    land(2);
+    cp_async_wait<0>();
+    land(3);
+    return true;
+  };
+  // This row's list entry for step gs of position gpos (fetched a step ahead of use).
+  auto entry = [&](int gpos, int gs) -> int {
+    const int j = gs * C::kRows + row;
+    return (gpos < p.npos && j < p.K) ? p.idx[static_cast<size_t>(gpos) * p.K + j] : -1;
+  };
   int item = 0, t = 0;
-  bool ok = true;
+  bool ok = p.npos > static_cast<int>(blockIdx.x) ? gather(blockIdx.x, 0, 0) : true;
+  int v_next = entry(blockIdx.x, 0);
   for (int pos = blockIdx.x; ok && pos < p.npos; pos += gridDim.x, ++item) {
-    const int32_t* list = p.idx + static_cast<size_t>(pos) * p.K;
     float lp[64];  // this row's share of each head's normaliser
 #pragma unroll
     for (int c = 0; c < 64; ++c) lp[c] = 0.f;
     for (int s = 0; s < nsteps; ++s, ++t) {
-      const int j = s * C::kRows + row;
-      const int v = (j < p.K) ? list[j] : -1;
+      const int v = v_next;
+      v_next = (s + 1 < nsteps) ? entry(pos, s + 1) : entry(pos + gridDim.x, 0);
       const bool valid = v >= 0 && v < p.N;
       if (!wait(C::kBarSF, t & 1, kSiteSoftSFull)) { ok = false; break; }
       float x[64];
@@ -365,6 +377,12 @@ __device__ __forceinline__ void topk_softmax(const TopkParams& p, uint32_t sbase
         tmem_st_wait();
       }
       warp_arrive(C::kBarPF);
+      // The next step's rows (of this position, or of the CTA's next one).
+      const int npos2 = (s + 1 < nsteps) ? pos : pos + static_cast<int>(gridDim.x);
+      if (npos2 < p.npos && !gather(npos2, (s + 1 < nsteps) ? s + 1 : 0, t + 1)) {
+        ok = false;
+        break;
+      }
     }
     if (!ok) break;
     // Position done: the normaliser of each head is the sum of lp over the 128 rows (and
@@ -416,12 +434,12 @@ __device__ __forceinline__ void topk_softmax(const TopkParams& p, uint32_t sbase
 // ------------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(TopkCfg::kThreads, 1)
-    bsa_topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                    const TopkParams p) {
+    bsa_topk_kernel(const __grid_constant__ CUtensorMap tm_q, const TopkParams p) {
   using C = TopkCfg;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned, by pointer arithmetic on the shared array itself, so that the
+  // compiler keeps shared-memory loads and stores (not generic ones) for it.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -430,14 +448,12 @@ __global__ void __launch_bounds__(TopkCfg::kThreads, 1)
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarPF || i == C::kBarOR || i == C::kBarG0 || i == C::kBarG1) ? 4 : 1);
+      mbar_init(bar(i), (i == C::kBarPF || i == C::kBarOR || i == C::kBarG0 || i == C::kBarG1 ||
+                       (i >= C::kBarKF && i < C::kBarKF + 4)) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_q);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(TopkCfg::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, p.expire_site};
   if (warp == 0) {
-    topk_producer(p, &tm_q, &tm_kv, sbase, ctl);
+    if (lane == 0) topk_producer(p, &tm_q, sbase, ctl);
   } else if (warp == 1) {
     if (lane == 0) topk_mma(p, sbase, tmem, ctl);
   } else {
