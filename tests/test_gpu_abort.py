@@ -101,3 +101,26 @@ def test_expired_rescale_wait():
     o1, l1 = bsa.forward(qd, kd, vd, lut, scale, block, True)
     assert lut.device_status()[0] == 0
     assert torch.equal(o1, o0) and torch.equal(l1, l0)
+
+
+@pytest.mark.parametrize("block", [128, 64])
+def test_backward_expired_wait_aborts_and_recovers(block):
+    """The backward's kernels take the same failure path: every wait site given up on
+    in turn, then a normal backward on the same LUT equals the one before."""
+    d = 128
+    q, k, v, lay, scale = _case(block, d)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    do = wls.randn_qkv(q.shape[0], q.shape[1], q.shape[2], d, seed=33)[0].cuda()
+    lut = bsa.build_lut(lay, q.shape[0])
+    o, lse = bsa.forward(qd, kd, vd, lut, scale, block, True)
+    g0 = [t.clone() for t in bsa.backward(qd, kd, vd, o, lse, do, lut, scale, block, True)]
+    assert lut.device_status()[0] == 0
+    for site in SITES:
+        lut.debug_expire_wait(site)
+        bsa.backward(qd, kd, vd, o, lse, do, lut, scale, block, True)
+        st, word = lut.device_status()
+        assert st == binding.BSA_ERR_DEVICE_TIMEOUT, (site, st, hex(word))
+        lut.debug_expire_wait(0)
+        g1 = bsa.backward(qd, kd, vd, o, lse, do, lut, scale, block, True)
+        assert lut.device_status()[0] == 0
+        assert all(torch.equal(a, b) for a, b in zip(g0, g1)), site
