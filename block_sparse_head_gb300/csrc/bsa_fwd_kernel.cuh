@@ -22,12 +22,15 @@
 //   warp 1      S issuer (one thread) and TMEM owner.  TMEM holds three S buffers and one
 //               O accumulator.  Step t: S(t) = Q K(t)^T into S[t % 3] once K(t) landed
 //               and PV(t-3), the last reader of that buffer, completed.
-//   last warp   PV issuer (one thread).  Step g: O += P(g) V(g), reading P from S[g % 3],
-//               once the softmax wrote P(g) and V(g) landed.
+//   warp 2      PV issuer (one thread).  Step g: O += P(g) V(g), reading P from S[g % 3],
+//               once the softmax wrote P(g) and V(g) landed (an item's first PV also
+//               once the epilogue read the previous item's O out).
 //               Two issuing threads keep the tensor pipe fed: it takes only a couple of
 //               MMAs ahead of issue, so a lone issuer idles it at every barrier check;
 //               the two streams order themselves through completion barriers only.
-//   softmax     b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
+//   warp 3      idle (completes the first warpgroup).
+//   softmax     warps 4-7 (and 8-11).
+//               b = 128: two warpgroups; each warp owns 16 TMEM lanes (rows) of its
 //               quadrant, lane t and t+16 holding the two 64-key halves of one row.
 //               b = 64 (M = 64 MMAs, rows in lanes 0-15 of each quadrant): one warpgroup,
 //               lane t and t+16 holding the step's two key blocks.  Per step: TMEM ->
@@ -36,10 +39,15 @@
 //               by three-input maxima and one shuffle, exp2(s*c - m) with the scale c =
 //               scale*log2(e) folded into a packed f32x2 FFMA), lazy rescale (the
 //               running max moves only when it grows by more than 2^8), P -> TMEM as bf16
-//               pairs over the S columns.  When an item ends its O is read out while the
-//               next item's first P is handed over, then normalised and stored as bf16
-//               with lse = ln 2 * (m + log2 l).  An item with no active block writes O = 0
-//               and lse = -inf.
+//               pairs over the S columns.  When an item ends, each row's (m, l) goes to
+//               the epilogue through shared memory; the softmax moves straight on.
+//   epilogue    the last warpgroup.  Per item: waits for the row statistics and the
+//               item's last PV, reads O out of TMEM (32x32b: one row per thread),
+//               releases the accumulator to the PV issuer, then stores O / l as bf16 and
+//               lse = ln 2 * (m + log2 l).  An item with no active block gets O = 0 and
+//               lse = -inf.
+//   At b = 128 the 16 warps are launched at 128 registers each and re-split per
+//   warpgroup with setmaxnreg (control 72, softmax 160, epilogue 120).
 // Work-list records (which carry each item's block indices, CSR row start and diagonal
 // position) are fetched two items ahead and column indices one step ahead of use, so no
 // role waits on a global load in its steady state.
@@ -71,8 +79,23 @@ struct FwdCfg {
   static_assert(KB == 64 || KB == 128, "key block must be 64 or 128");
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kNumWG = (QB == 128) ? 2 : 1;  // softmax warpgroups
-  static constexpr int kPvWarp = 2 + 4 * kNumWG;       // after the softmax warps
-  static constexpr int kThreads = 32 * (kPvWarp + 1);  // producer, S issuer, softmax, PV issuer
+  // QB = 128: an epilogue warpgroup reads O out and stores it.  QB = 64 (one softmax
+  // warpgroup, items of many steps): the softmax does it at the next item's first step.
+  static constexpr bool kEpi = (QB == 128);
+  static constexpr int kSoftWarp = 4;                  // first softmax warp
+  static constexpr int kEpiWarp = 4 + 4 * kNumWG;      // first epilogue warp
+  static constexpr int kThreads = 32 * (kEpiWarp + (kEpi ? 4 : 0));
+  // The epilogue spaces its 32-byte stores of a row this far apart: a burst of an item's
+  // 32 KB of stores stalls the softmax warps' next step by about a thousand cycles.
+  static constexpr unsigned kStoreGapNs = 150;
+  // Registers per thread after the split (b = 128): the launch gives every thread
+  // 65536 / 512 = 128; the control and epilogue warpgroups hand 56 and 8 to each
+  // softmax thread.
+  static constexpr bool kSplitRegs = (QB == 128);
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kRegCtl = 72, kRegSoft = 160, kRegEpi = 120;
+  static_assert(!kSplitRegs || kRegCtl + kNumWG * kRegSoft + kRegEpi == 4 * kLaunchRegs,
+                "register split must add up to the launch's registers");
   static constexpr int kKR = 128;                 // key rows per step
   static constexpr int kG = kKR / KB;             // blocks per step (1 or 2)
   static constexpr int kNS = 3;                   // S buffers = stage barriers in flight
@@ -105,10 +128,14 @@ struct FwdCfg {
   static constexpr int kBarPF = 12;               // [3] P(g) written, O free (one arrive per softmax warp)
   static constexpr int kBarDrainS = 15;
   static constexpr int kBarDrainP = 16;
-  static constexpr int kNumBars = 17;
+  static constexpr int kBarOFree = 17;            // O read out (one arrive per epilogue warp)
+  static constexpr int kBarStFull = 18;           // row statistics written (per softmax warp)
+  static constexpr int kBarStFree = 19;           // row statistics read (per epilogue warp)
+  static constexpr int kNumBars = 20;
   static constexpr int kBarBytes = 192;           // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
-  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + align slack
+  static constexpr int kOffStats = kOffBar + kBarBytes;  // float2 (m, l) per row
+  static constexpr int kSmemBytes = kOffStats + QB * 8 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // Launch request: more than half of the SM's shared memory, so that two CTAs never
   // share an SM (each allocates all 512 TMEM columns; a second one would stall in
@@ -119,6 +146,15 @@ struct FwdCfg {
   static constexpr uint32_t kIdescS1 = idesc_bf16_f32(QB, KB, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(QB, D, false, true);
 };
+
+// Bounded wait: with the slow path inline where registers are re-split per warpgroup
+// (no calls there), out of line elsewhere (smaller code).
+template <bool kInline>
+__device__ __forceinline__ bool fwd_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                         int site) {
+  if constexpr (kInline) return mbar_wait_inl(bar, parity, ctl, site);
+  else return mbar_wait(bar, parity, ctl, site);
+}
 
 // Blocks in step s of a row with nnz active blocks.
 template <int G>
@@ -259,7 +295,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       // issue order, so one wait covers all of it.
       int j = (t >= 3) ? t - 3 : -1;
       if (first) j = max(j, t - (C::kNQ == 1 ? 1 : 2));
-      if (j >= 0 && !mbar_wait(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
+      if (j >= 0 && !fwd_wait<C::kSplitRegs>(bar(C::kBarSF + j % 3), (j / 3) & 1, ctl, kSiteProdKEmpty)) break;
       const uint32_t fb = bar(C::kBarKF + t % 3);
       mbar_arrive_expect_tx(fb, (first ? C::kQTile : 0) + r0.nblk * C::kBlkB);
       ++nk;
@@ -276,7 +312,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const CUtensorM
       // issued after taking that V barrier phase.
       const int g = t - 2;
       const int gv = g - C::kNV;
-      if (gv >= 0 && !mbar_wait(bar(C::kBarPVD + gv % 3), (gv / 3) & 1, ctl, kSiteProdVEmpty))
+      if (gv >= 0 && !fwd_wait<C::kSplitRegs>(bar(C::kBarPVD + gv % 3), (gv / 3) & 1, ctl, kSiteProdVEmpty))
         break;
       const uint32_t fb = bar(C::kBarVF + g % 3);
       mbar_arrive_expect_tx(fb, rv.nblk * C::kBlkB);
@@ -329,9 +365,9 @@ __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, ui
     const int nblk = c.nblk();
     const int qb = c.is.n % C::kNQ;
     c.advance(p);
-    if (!mbar_wait(bar(C::kBarKF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
+    if (!fwd_wait<C::kSplitRegs>(bar(C::kBarKF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
     // S[t % 3] was last read by PV(t-3).
-    if (t >= 3 && !mbar_wait(bar(C::kBarPVD + t % 3), ((t - 3) / 3) & 1, ctl, kSiteMmaPvDone)) break;
+    if (t >= 3 && !fwd_wait<C::kSplitRegs>(bar(C::kBarPVD + t % 3), ((t - 3) / 3) & 1, ctl, kSiteMmaPvDone)) break;
     tc_fence_after();
     const uint32_t sb = tmem + (t % 3) * 128;
     const uint32_t qlo = md.q0 + qb * (C::kQTile >> 4);
@@ -373,10 +409,17 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
   for (int g = 0; c.valid(); ++g) {
     const int nblk = c.nblk();
     const bool first = (c.s == 0);
+    const int item = c.is.n;  // among the non-empty items
     c.advance(p);
-    // P(g) written (and, on an item's first step, O read out), V(g) landed.
-    if (!mbar_wait(bar(C::kBarPF + g % 3), (g / 3) & 1, ctl, kSiteMmaPFull)) break;
-    if (!mbar_wait(bar(C::kBarVF + g % 3), (g / 3) & 1, ctl, kSiteMmaStage)) break;
+    // P(g) written, V(g) landed; on an item's first step, the previous item's O read out
+    // (the epilogue releases O once per item, after this thread issued that item's PVs,
+    // so its barrier cannot be a phase ahead; without an epilogue the softmax reads O
+    // out before it hands that step's P over).
+    if (!fwd_wait<C::kSplitRegs>(bar(C::kBarPF + g % 3), (g / 3) & 1, ctl, kSiteMmaPFull)) break;
+    if (!fwd_wait<C::kSplitRegs>(bar(C::kBarVF + g % 3), (g / 3) & 1, ctl, kSiteMmaStage)) break;
+    if (C::kEpi && first && item > 0 &&
+        !fwd_wait<C::kSplitRegs>(bar(C::kBarOFree), (item - 1) & 1, ctl, kSiteMmaORead))
+      break;
     tc_fence_after();
     const uint32_t ps = tmem + (g % 3) * 128;
     const uint32_t od = tmem + C::kOCol;
@@ -407,7 +450,8 @@ __device__ __forceinline__ void store_o32(uint32_t to, int c, const uint32_t (&r
   tmem_st_16x32bx2_x32<32>(to + c * 64, r);
 }
 
-// Reads this thread's half row of O, scales it by inv and packs it to bf16 pairs.
+// Reads this thread's half row of O (the load_o32 groups), scales it by inv and packs it
+// to bf16 pairs.
 template <int D>
 __device__ __forceinline__ void read_o(uint32_t to, float inv, uint32_t (&pk)[D / 4]) {
   constexpr int OC = D / 2;
@@ -465,17 +509,16 @@ __device__ __forceinline__ float finish_row(float& m, float& l, float t) {
 }
 
 template <int QB, int KB, int D, bool EXT>
-__device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, uint32_t tmem,
-                                            const WaitCtl& ctl) {
+__device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, uint8_t* smem,
+                                            uint32_t tmem, const WaitCtl& ctl) {
   using C = FwdCfg<QB, KB, D>;
   constexpr int G = C::kG;
   constexpr int NC = 64;      // score columns per thread
   constexpr int OC = D / 2;   // O columns per thread
   constexpr int NA = 8;       // independent max chains
   constexpr int NS = 4;       // packed sum accumulators
-  constexpr float kLog2e = 1.4426950408889634f;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
-  const int wg = ((threadIdx.x >> 5) - 2) >> 2;  // softmax group (warps 2-5, 6-9)
+  const int wg = ((threadIdx.x >> 5) - C::kSoftWarp) >> 2;  // softmax group (warps 4-7, 8-11)
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
@@ -486,7 +529,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   // This half holds keys [64*half, 64*half + 64) of the step: half of the block when
   // KB = 128, block `half` of the step (all of its 64 keys) when KB = 64.
   const int kbase = (KB == 128) ? 64 * half : 0;
+  float2* stats = reinterpret_cast<float2*>(smem + C::kOffStats);
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+  constexpr float kLog2e = 1.4426950408889634f;
   // scale > 0: the row max of the raw scores gives the max of the scaled ones and the
   // exponent is one FFMA.  Otherwise (and always in the extended kernels, which transform
   // the scores first) the scores are scaled first (c = 1 afterwards).
@@ -494,6 +539,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   const float cs = pos_scale ? p.scale_log2 : 1.f;
   int g = 0;
   bool ok = true;
+  // Without an epilogue: the previous item's row, O read out at this item's first step.
   bool have_pending = false;
   int pend_row = 0;
   float pend_m = 0.f, pend_l = 0.f;
@@ -511,17 +557,18 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
   };
   // Waits (bounded, warp-uniform result) for phase `parity` of barrier b.
   auto wait_bar = [&](int b, int parity, int site) -> bool {
-    bool w = mbar_wait(bar(b), parity, ctl, site);
+    bool w = fwd_wait<C::kSplitRegs>(bar(b), parity, ctl, site);
     w = __all_sync(0xffffffffu, w);
     if (w) tc_fence_after();
     return w;
   };
 
+  // With an epilogue, items with no active block are the epilogue's alone.
   ItemStream is;
-  for (is.init<false>(p); ok && !is.done(); is.next<false>(p)) {
+  for (is.init<C::kEpi>(p); ok && !is.done(); is.next<C::kEpi>(p)) {
     const int nnz = is.nnz();
     const int qrow = is.cur.x * p.Lq + is.cur.y * QB + row;  // global query row
-    // (EXT) the row's position in its sequence, batch, head, segment and sink
+    // (EXT) the row's position in its sequence, batch, segment and sink
     int qpos = 0, qseg = 0;
     bool row_ok = true;
     float sink_t = -INFINITY;
@@ -530,13 +577,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       qpos = is.cur.y * QB + row;
       row_ok = qpos < p.Lq;
       const int bi = is.cur.x / p.H;
-      if (p.sinks != nullptr) sink_t = p.sinks[is.cur.x - bi * p.H] * kLog2e;
+      if (!C::kEpi && p.sinks != nullptr) sink_t = p.sinks[is.cur.x - bi * p.H] * kLog2e;
       if (p.kv_seg != nullptr) {
         kvseg = p.kv_seg + static_cast<size_t>(bi) * p.Lk;
         qseg = row_ok ? p.q_seg[static_cast<size_t>(bi) * p.Lq + qpos] : 0;
       }
     }
-    if (nnz == 0) {
+    if (!C::kEpi && nnz == 0) {
       if (row_ok) {
         uint4* orow = reinterpret_cast<uint4*>(outp + static_cast<size_t>(qrow) * D + half * OC);
 #pragma unroll
@@ -693,10 +740,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
           store_o32(to, c, r);
         }
       }
-      // First step of an item: the previous item's O (its last PV is g-1) is read out
-      // before this P is handed over, since the next PV overwrites O.
+      // Without an epilogue, at an item's first step: the previous item's O (its last
+      // PV is g-1) is read out before this P is handed over, since the next PV
+      // overwrites O.
       uint32_t opk[D / 4];
-      if (s == 0 && have_pending) {
+      if (!C::kEpi && s == 0 && have_pending) {
         ok = wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone);
         if (!ok) break;
         const float inv = EXT ? finish_row(pend_m, pend_l, pend_t)
@@ -705,26 +753,137 @@ __device__ __forceinline__ void fwd_softmax(const FwdParams& p, uint32_t sbase, 
       }
       tmem_st_wait();
       warp_arrive(C::kBarPF + g % 3);
-      if (s == 0 && have_pending) {
+      if (!C::kEpi && s == 0 && have_pending) {
         if (pend_ok) store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
         have_pending = false;
       }
     }
     if (!ok) break;
-    pend_row = qrow;
-    pend_m = m_used;
-    pend_l = l;
-    pend_ok = row_ok;
-    pend_t = sink_t;
-    have_pending = true;
+    if constexpr (C::kEpi) {
+      // Row statistics to the epilogue, once it has read the previous item's (both
+      // barriers complete once per item, so neither can be a phase ahead of its waiter).
+      if (is.n > 0) {
+        ok = wait_bar(C::kBarStFree, (is.n - 1) & 1, kSiteSoftStatsFree);
+        if (!ok) break;
+      }
+      if (half == 0) stats[row] = make_float2(m_used, l);
+      __threadfence_block();
+      warp_arrive(C::kBarStFull);
+    } else {
+      pend_row = qrow;
+      pend_m = m_used;
+      pend_l = l;
+      pend_ok = row_ok;
+      pend_t = sink_t;
+      have_pending = true;
+    }
   }
-  if (ok && have_pending &&
+  if (!C::kEpi && ok && have_pending &&
       wait_bar(C::kBarPVD + (g - 1) % 3, ((g - 1) / 3) & 1, kSiteSoftItemDone)) {
     uint32_t opk[D / 4];
     const float inv = EXT ? finish_row(pend_m, pend_l, pend_t)
                           : ((pend_l > 0.f) ? 1.f / pend_l : 0.f);
     read_o<D>(to, inv, opk);
     if (pend_ok) store_o<D>(p, pend_row, half, opk, pend_m, pend_l);
+  }
+}
+
+// ----------------------------------------------------------------- epilogue
+
+// Per item: the rows' (m, l) from the softmax, O out of TMEM once the item's last PV is
+// done (one row per thread, 32x32b; at QB = 64 the rows sit in lanes 0-15 of each
+// quadrant), O released to the PV issuer, then O / l stored as bf16 and the lse.
+template <int QB, int KB, int D, bool EXT>
+__device__ __forceinline__ void fwd_epilogue(const FwdParams& p, uint32_t sbase, const uint8_t* smem,
+                                             uint32_t tmem, const WaitCtl& ctl) {
+  using C = FwdCfg<QB, KB, D>;
+  constexpr int G = C::kG;
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.6931471805599453f;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int lane = threadIdx.x & 31;
+  const bool lane_row = (QB == 128) || lane < 16;
+  const int row = (QB == 128) ? wq * 32 + lane : wq * 16 + (lane & 15);
+  const uint32_t to = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kOCol;
+  const float2* stats = reinterpret_cast<const float2*>(smem + C::kOffStats);
+  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
+  const bool v8 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
+  auto wait_bar = [&](int b, int parity, int site) -> bool {
+    bool w = fwd_wait<C::kSplitRegs>(bar(b), parity, ctl, site);
+    w = __all_sync(0xffffffffu, w);
+    if (w) tc_fence_after();
+    return w;
+  };
+  auto warp_arrive = [&](int b) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(b));
+  };
+
+  int g = 0;  // first step of the current item
+  ItemStream is;
+  for (is.init<false>(p); !is.done(); is.next<false>(p)) {
+    const int nnz = is.nnz();
+    const int qrow = is.cur.x * p.Lq + is.cur.y * QB + row;  // global query row
+    bool row_ok = lane_row;
+    float sink_t = -INFINITY;  // (EXT) sink logit, log2 units
+    if constexpr (EXT) {
+      row_ok = row_ok && (is.cur.y * QB + row < p.Lq);
+      if (p.sinks != nullptr) sink_t = p.sinks[is.cur.x % p.H] * kLog2e;
+    }
+    __nv_bfloat16* orow = outp + static_cast<size_t>(qrow) * D;
+    if (nnz == 0) {
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+        p.lse[qrow] = (sink_t == -INFINITY) ? -INFINITY : sink_t / kLog2e;
+      }
+      continue;
+    }
+    const int gl = g + (nnz + G - 1) / G - 1;  // the item's last step
+    g = gl + 1;
+    if (!wait_bar(C::kBarStFull, is.n & 1, kSiteEpiStats)) break;
+    const float2 ml = stats[row];
+    warp_arrive(C::kBarStFree);
+    // PV(gl)'s barrier cannot move on to PV(gl+3): the next item's first PV waits for
+    // the O release below.
+    if (!wait_bar(C::kBarPVD + gl % 3, (gl / 3) & 1, kSiteSoftItemDone)) break;
+    float m = ml.x, l = ml.y;
+    const float inv = EXT ? finish_row(m, l, sink_t) : ((l > 0.f) ? 1.f / l : 0.f);
+    uint32_t pk[D / 2];
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(to + h * 64, r0);
+      tmem_ld_32x32b_x32(to + h * 64 + 32, r1);
+      tmem_ld_wait(r0);
+      tmem_ld_wait(r1);
+      if (h == D / 64 - 1) warp_arrive(C::kBarOFree);  // O may be overwritten now
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        pk[h * 32 + i] = pack_bf16x2(__uint_as_float(r0[2 * i]) * inv,
+                                     __uint_as_float(r0[2 * i + 1]) * inv);
+        pk[h * 32 + 16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]) * inv,
+                                          __uint_as_float(r1[2 * i + 1]) * inv);
+      }
+    }
+    if (row_ok) {
+      if (v8) {
+#pragma unroll
+        for (int q = 0; q < D / 16; ++q) {
+          if (q > 0) __nanosleep(C::kStoreGapNs);
+          st_global_v8(orow + q * 16, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3],
+                       pk[8 * q + 4], pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q)
+          reinterpret_cast<uint4*>(orow)[q] =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+      p.lse[qrow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
   }
 }
 
@@ -755,6 +914,9 @@ __global__ void __launch_bounds__(FwdCfg<QB, KB, D>::kThreads, 1)
     }
     mbar_init(bar(C::kBarDrainS), 1);
     mbar_init(bar(C::kBarDrainP), 1);
+    mbar_init(bar(C::kBarOFree), 4);
+    mbar_init(bar(C::kBarStFull), 4 * C::kNumWG);
+    mbar_init(bar(C::kBarStFree), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -773,14 +935,21 @@ __global__ void __launch_bounds__(FwdCfg<QB, KB, D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns, p.expire_site};
 
-  if (warp == 0) {
-    if (lane == 0) fwd_producer<QB, KB, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
-  } else if (warp == 1) {
-    if (lane == 0) fwd_mma_s<QB, KB, D>(p, sbase, tmem, ctl);
-  } else if (warp == C::kPvWarp) {
-    if (lane == 0) fwd_mma_pv<QB, KB, D>(p, sbase, tmem, ctl);
-  } else {
-    fwd_softmax<QB, KB, D, EXT>(p, sbase, tmem, ctl);
+  if (warp < C::kSoftWarp) {
+    if constexpr (C::kSplitRegs) setmaxnreg_dec<C::kRegCtl>();
+    if (warp == 0) {
+      if (lane == 0) fwd_producer<QB, KB, D>(p, &tm_q, &tm_k, &tm_v, sbase, ctl);
+    } else if (warp == 1) {
+      if (lane == 0) fwd_mma_s<QB, KB, D>(p, sbase, tmem, ctl);
+    } else if (warp == 2) {
+      if (lane == 0) fwd_mma_pv<QB, KB, D>(p, sbase, tmem, ctl);
+    }
+  } else if (warp < C::kEpiWarp) {
+    if constexpr (C::kSplitRegs) setmaxnreg_inc<C::kRegSoft>();
+    fwd_softmax<QB, KB, D, EXT>(p, sbase, smem, tmem, ctl);
+  } else if constexpr (C::kEpi) {
+    if constexpr (C::kSplitRegs) setmaxnreg_dec<C::kRegEpi>();
+    fwd_epilogue<QB, KB, D, EXT>(p, sbase, smem, tmem, ctl);
   }
 
   tc_fence_before();
@@ -804,6 +973,14 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& q, const CUtensorM
     e = cudaFuncSetAttribute(bsa_fwd_kernel<QB, KB, D, EXT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchSmem);
     if (e != cudaSuccess) return e;
+    if (C::kSplitRegs) {
+      // setmaxnreg.inc waits for registers that the other warpgroups gave back: the
+      // shares only add up when the kernel is launched at exactly kLaunchRegs.
+      cudaFuncAttributes fa{};
+      e = cudaFuncGetAttributes(&fa, bsa_fwd_kernel<QB, KB, D, EXT>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
   bsa_fwd_kernel<QB, KB, D, EXT><<<grid, C::kThreads, C::kLaunchSmem, stream>>>(q, k, v, p);

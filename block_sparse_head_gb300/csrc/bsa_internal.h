@@ -80,8 +80,11 @@ enum WaitSite : int {
   kSiteMmaPFull = 7,
   kSiteMmaPvDone = 8,
   kSiteSoftSFull = 9,
+  kSiteMmaORead = 10,
   kSiteSoftPvDone = 11,
   kSiteSoftItemDone = 12,
+  kSiteEpiStats = 13,
+  kSiteSoftStatsFree = 14,
   kSiteSelftest = 15,
 };
 

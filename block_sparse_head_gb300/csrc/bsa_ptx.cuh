@@ -77,8 +77,8 @@ struct WaitCtl {
 
 constexpr int kStatusTimeout = 0x10000;
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
-                                            int site) {
+__device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                                int site) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -91,6 +91,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
       return false;
     }
   }
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                            int site) {
+  return mbar_wait_timed(bar, parity, ctl, site);
 }
 
 // The common case (the phase completes within a few microseconds) stays inline and never
@@ -111,6 +116,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, ctl, site);
+}
+
+// The same wait with nothing out of line, for kernels that re-split registers per
+// warpgroup (setmaxnreg): ptxas cannot allocate registers around a call there.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                              int site) {
+  if (site == ctl.expire_site) {
+    atomicCAS(ctl.status, 0, kStatusTimeout | site);
+    *ctl.abort_flag = 1;
+    return false;
+  }
+  if (mbar_test_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_timed(bar, parity, ctl, site);
 }
 
 // Bounded wait that ignores the abort flag and never records a status: used only
@@ -271,6 +292,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void tmem_st_wait() {

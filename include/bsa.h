@@ -372,8 +372,11 @@ int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns);
  * forward are undefined; bsa_device_status reports it.  site 0 turns the knob off.
  * Site ids (low 16 bits of the status word): 1 producer, K slot free; 2 producer, V
  * slot free; 6 MMA issuers, K or V landed; 7 PV issuer, P written; 8 S issuer, S
- * buffer free; 9 softmax, S computed; 11 softmax, O free for a rescale; 12 softmax,
- * the item's last PV done.  Errors: BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (site outside
+ * buffer free; 9 softmax, S computed; 10 PV issuer, the previous item's O read out;
+ * 11 softmax, O free for a rescale; 12 the item's last PV done (forward: epilogue at
+ * block 128, softmax at block 64; backward: softmax); 13 epilogue, the rows'
+ * statistics written; 14 softmax, the previous rows' statistics read (sites 10, 13
+ * and 14: the forward at block 128 only).  Errors: BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (site outside
  * [0, 65535]).
  */
 int bsa_debug_expire_wait(bsa_lut* lut, int site);
