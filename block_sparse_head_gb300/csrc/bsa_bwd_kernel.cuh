@@ -20,17 +20,22 @@
 //
 // GB300 mapping.  One CTA per SM, persistent over its share of the work list (the same
 // longest-first per-CTA schedule as the forward):
-//   warp 0      TMA producer: item tiles (one 3-D copy each) and step tiles into two
-//               stages; in dK/dV mode also the step's lse and delta (bulk copies).
-//   warp 1      MMA issuer (one thread) and TMEM owner: T1 (128 columns), T2 (128), acc1
-//               (d) and, in dK/dV mode, acc2 (d) -- 512 columns at d = 128.
+//   warp 0      TMA producer: item tiles (one 3-D copy each) and step tiles; in dK/dV mode
+//               X and Y in two stages plus the step's lse and delta (bulk copies), in dQ
+//               mode X (= K) in a ring of three and Y (= V) in a ring of two.
+//   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2..   elementwise warpgroups (two at b = 128, one at b = 64), laid out as the
 //               forward's softmax: per step they read T1 and T2, form P and dS, and write
 //               the bf16 operands E1 (over T1) and E2 (over T2) for the second MMAs.  At an
 //               item's end they read the accumulators, scale and store them as bf16.
-// Each step runs MMA1/MMA2 -> elementwise -> MMA3/MMA4 in order (T1/T2 are single
-// buffered); the step tiles of the next step load meanwhile.  Every wait is bounded
-// (WaitCtl), as in the forward.
+// dK/dV mode: T1 (128 columns), T2 (128), acc1 and acc2 (d each) fill the 512 columns, so
+// each step runs MMA1/MMA2 -> elementwise -> MMA3/MMA4 in order.
+// dQ mode: T1 alternates between two 128-column regions (steps of even and odd index)
+// beside T2 and acc1.  MMA1 of step t goes in as soon as MMA3 of step t-2 has read its
+// region, so it runs while the elementwise warps work on step t-1; MMA3 of step t-1 goes in
+// after MMA2 of step t, so it runs while they work on step t.  An item's accumulator is
+// read out at the next item's first step, after that step's operands are handed over.
+// Every wait is bounded (WaitCtl), as in the forward.
 #pragma once
 
 #include "bsa_fwd_kernel.cuh"
@@ -49,32 +54,37 @@ struct BwdCfg {
   static constexpr int kStepTile = 128 * D * 2;  // one step tile (X or Y), kG blocks
   static constexpr int kBlkB = BLK * D * 2;      // one block of a step tile
   static constexpr int kHalf = BLK * 128;        // one 64-column half of one block
+  static constexpr int kNX = KV ? 2 : 3;  // X slots (dQ mode: K, held until MMA3 one step on)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kItemTile;
-  static constexpr int kOffX = 2 * kItemTile;            // [2] stages
-  static constexpr int kOffY = kOffX + 2 * kStepTile;    // [2] stages
-  static constexpr int kOffVec = kOffY + 2 * kStepTile;  // [2] stages x {lse, delta}[128] fp32
+  static constexpr int kOffX = 2 * kItemTile;              // [kNX] slots
+  static constexpr int kOffY = kOffX + kNX * kStepTile;    // [2] slots
+  static constexpr int kOffVec = kOffY + 2 * kStepTile;    // [2] stages x {lse, delta}[128] fp32
   static constexpr int kVecBytes = KV ? 2 * 2 * 128 * 4 : 0;
   static constexpr int kOffBar = kOffVec + kVecBytes;
   // barriers
   static constexpr int kBarIF = 0;    // item tiles landed
   static constexpr int kBarIE = 1;    // item tiles free (the item's last MMA1/MMA2 done)
-  static constexpr int kBarXF = 2;    // [2] step tiles landed
-  static constexpr int kBarXE = 4;    // [2] step tiles free (the step's MMA3/MMA4 done)
-  static constexpr int kBarTF = 6;    // T1, T2 computed
-  static constexpr int kBarEF = 7;    // E1 (E2) written (one arrive per elementwise warp)
-  static constexpr int kBarAD = 8;    // the step's MMA3/MMA4 done
-  static constexpr int kBarAR = 9;    // accumulators read out (one arrive per elementwise warp)
-  static constexpr int kBarDrain = 10;
-  static constexpr int kNumBars = 11;
-  static constexpr int kBarBytes = 128;  // barriers, TMEM slot, abort flag
+  static constexpr int kBarXF = 2;    // [kNX] X landed (dK/dV mode: X, Y and the vectors)
+  static constexpr int kBarXE = 5;    // [kNX] X free (its step's MMA3 (and MMA4) done)
+  static constexpr int kBarYF = 8;    // [2] dQ mode: Y landed
+  static constexpr int kBarYE = 10;   // [2] dQ mode: Y free (its step's MMA2 done)
+  static constexpr int kBarTF = 12;   // T1, T2 computed
+  static constexpr int kBarEF = 13;   // E1 (E2) written (one arrive per elementwise warp)
+  static constexpr int kBarAD = 14;   // [2] a step's MMA3/MMA4 done (dQ mode: by T1 region)
+  static constexpr int kBarAR = 16;   // accumulators read out (one arrive per elementwise warp)
+  static constexpr int kBarDrain = 17;
+  static constexpr int kNumBars = 18;
+  static constexpr int kBarBytes = 192;  // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr int kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
-  // TMEM columns
-  static constexpr int kT1 = 0, kT2 = 128, kAcc1 = 256, kAcc2 = 256 + D;
-  static_assert(kAcc2 + (KV ? D : 0) <= 512, "TMEM budget");
+  // TMEM columns.  dQ mode: T1 at 0 (even steps) or 256 (odd steps), T2 at 128, acc1 at
+  // 384.  dK/dV mode: T1 at 0, T2 at 128, acc1 at 256, acc2 after it.
+  static constexpr int kT1 = 0, kT2 = 128, kT1b = 256;
+  static constexpr int kAcc1 = KV ? 256 : 384, kAcc2 = 256 + D;
+  static_assert(KV ? (kAcc2 + D <= 512) : (kAcc1 + D <= 512), "TMEM budget");
   static constexpr uint32_t kIdesc1 = idesc_bf16_f32(BLK, 128, false, false);  // N = 128
   static constexpr uint32_t kIdesc1b = idesc_bf16_f32(BLK, BLK, false, false); // one block
   static constexpr uint32_t kIdesc3 = idesc_bf16_f32(BLK, D, false, true);     // B MN-major
@@ -114,6 +124,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
   StepCursor<G> c;
   c.init(p);
   int n = -1, t = 0;
+  int nx = 0, ny = 0;  // dQ mode: steps whose X (Y) copies were armed
   bool ok = true;
   for (; c.valid(); ++t) {
     const int nblk = c.nblk();
@@ -136,32 +147,62 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
       tma_load_3d(sbase + C::kOffB, tm_b, fb, 0, row, 0);
     }
     c.advance(p);
-    // Step stage t % 2 held step t-2, read by its MMA3/MMA4.
-    if (t >= 2 && !mbar_wait(bar(C::kBarXE + t % 2), ((t - 2) / 2) & 1, ctl, kSiteProdVEmpty)) {
-      ok = false;
-      break;
-    }
-    const uint32_t fb = bar(C::kBarXF + t % 2);
-    mbar_arrive_expect_tx(fb, nblk * (2 * C::kBlkB + (KV ? 2 * BLK * 4 : 0)));
-    const uint32_t xd = sbase + C::kOffX + (t % 2) * C::kStepTile;
-    const uint32_t yd = sbase + C::kOffY + (t % 2) * C::kStepTile;
+    if constexpr (KV) {
+      // Step stage t % 2 held step t-2, read by its MMA3/MMA4.
+      if (t >= 2 && !mbar_wait(bar(C::kBarXE + t % 2), ((t - 2) / 2) & 1, ctl, kSiteProdVEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = bar(C::kBarXF + t % 2);
+      mbar_arrive_expect_tx(fb, nblk * (2 * C::kBlkB + 2 * BLK * 4));
+      const uint32_t xd = sbase + C::kOffX + (t % 2) * C::kStepTile;
+      const uint32_t yd = sbase + C::kOffY + (t % 2) * C::kStepTile;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (g < nblk) {
-        const int row = bh * p.L + cols[g] * BLK;
-        tma_load_3d(xd + g * C::kBlkB, tm_x, fb, 0, row, 0);
-        tma_load_3d(yd + g * C::kBlkB, tm_y, fb, 0, row, 0);
-        if constexpr (KV) {
+      for (int g = 0; g < G; ++g) {
+        if (g < nblk) {
+          const int row = bh * p.L + cols[g] * BLK;
+          tma_load_3d(xd + g * C::kBlkB, tm_x, fb, 0, row, 0);
+          tma_load_3d(yd + g * C::kBlkB, tm_y, fb, 0, row, 0);
           const uint32_t vd = sbase + C::kOffVec + (t % 2) * 1024 + g * BLK * 4;
           bulk_load(vd, p.lse + row, BLK * 4, fb);
           bulk_load(vd + 512, p.delta + row, BLK * 4, fb);
         }
       }
+    } else {
+      // X slot t % 3 held K(t-3), read by MMA3(t-3); Y slot t % 2 held V(t-2), read by
+      // MMA2(t-2).
+      if (t >= 3 && !mbar_wait(bar(C::kBarXE + t % 3), ((t - 3) / 3) & 1, ctl, kSiteProdKEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fx = bar(C::kBarXF + t % 3);
+      mbar_arrive_expect_tx(fx, nblk * C::kBlkB);
+      const uint32_t xd = sbase + C::kOffX + (t % 3) * C::kStepTile;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (g < nblk) tma_load_3d(xd + g * C::kBlkB, tm_x, fx, 0, bh * p.L + cols[g] * BLK, 0);
+      ++nx;
+      if (t >= 2 && !mbar_wait(bar(C::kBarYE + t % 2), ((t - 2) / 2) & 1, ctl, kSiteProdVEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fy = bar(C::kBarYF + t % 2);
+      mbar_arrive_expect_tx(fy, nblk * C::kBlkB);
+      const uint32_t yd = sbase + C::kOffY + (t % 2) * C::kStepTile;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (g < nblk) tma_load_3d(yd + g * C::kBlkB, tm_y, fy, 0, bh * p.L + cols[g] * BLK, 0);
+      ++ny;
     }
   }
-  (void)ok;
   // Wait for every copy this thread issued (immediate on the normal path).
-  for (int j = (t > 2 ? t - 2 : 0); j < t; ++j) mbar_drain_wait(bar(C::kBarXF + j % 2), (j / 2) & 1);
+  if constexpr (KV) {
+    for (int j = (t > 2 ? t - 2 : 0); j < t; ++j) mbar_drain_wait(bar(C::kBarXF + j % 2), (j / 2) & 1);
+  } else {
+    for (int j = (nx > 3 ? nx - 3 : 0); j < nx; ++j) mbar_drain_wait(bar(C::kBarXF + j % 3), (j / 3) & 1);
+    for (int j = (ny > 2 ? ny - 2 : 0); j < ny; ++j) mbar_drain_wait(bar(C::kBarYF + j % 2), (j / 2) & 1);
+  }
+  (void)ok;
   if (n >= 0) mbar_drain_wait(bar(C::kBarIF), n & 1);
 }
 
@@ -188,65 +229,144 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   constexpr uint32_t kStage = C::kStepTile >> 4;
   const uint32_t t1 = tmem + C::kT1, t2 = tmem + C::kT2;
   const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
-
-  StepCursor<G> c;
-  c.init(p);
-  int n = -1;
-  for (int t = 0; c.valid(); ++t) {
-    const int nblk = c.nblk();
-    const bool first = c.s == 0;
-    const bool last = c.s == c.nsteps - 1;
-    c.advance(p);
-    if (first) {
-      ++n;
-      if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) break;
-    }
-    if (!mbar_wait(bar(C::kBarXF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) break;
-    // T1/T2 are free once the previous step's MMA3/MMA4 have read E1/E2 from them.
-    if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
-    tc_fence_after();
-    const uint32_t xs = x0 + (t % 2) * kStage, ys = y0 + (t % 2) * kStage;
+  // T = item tile (A or B) x step tile^T over d: one N = 128 MMA per 16 columns of d, or
+  // one N = 64 MMA per block at b = 64.
+  auto issue_first = [&](uint32_t td, uint32_t it, uint32_t st, int nblk) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
       const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
       if (BLK == 128) {
-        tc_mma_ss_lh(t1, a0 + ia, hi, xs + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
-        tc_mma_ss_lh(t2, b0 + ia, hi, ys + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+        tc_mma_ss_lh(td, it + ia, hi, st + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
       } else {
 #pragma unroll
         for (int g = 0; g < G; ++g)
-          if (g < nblk) {
-            const uint32_t go = (g * C::kBlkB) >> 4;
-            tc_mma_ss_lh(t1 + g * BLK, a0 + ia, hi, xs + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
-            tc_mma_ss_lh(t2 + g * BLK, b0 + ia, hi, ys + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
-          }
+          if (g < nblk)
+            tc_mma_ss_lh(td + g * BLK, it + ia, hi, st + is + ((g * C::kBlkB) >> 4), hi,
+                         C::kIdesc1b, kk > 0 ? 1u : 0u);
       }
     }
-    tc_commit(bar(C::kBarTF));
-    if (last) tc_commit(bar(C::kBarIE));
-    if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
-    // An item's first accumulation overwrites the accumulators: the previous item's must
-    // have been read out.
-    if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
-    tc_fence_after();
-    const uint32_t xm = xm0 + (t % 2) * kStage, ym = ym0 + (t % 2) * kStage;
+  };
+  // acc += E (bf16 in TMEM, 128 columns of the step) x step tile (MN-major).
+  auto issue_second = [&](uint32_t acc, uint32_t te, uint32_t sm, int nblk, bool first) {
     const int ksteps = nblk * BLK / 16;
 #pragma unroll
     for (int kk = 0; kk < 128 / 16; ++kk) {
       if (kk < ksteps) {
         const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-        const uint32_t accum = (first && kk == 0) ? 0u : 1u;
-        if constexpr (KV) {
-          tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
-          tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
-        } else {
-          tc_mma_ts_lh(acc1, t1 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dQ += dS K
-        }
+        tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
       }
     }
-    tc_commit(bar(C::kBarAD));
-    tc_commit(bar(C::kBarXE + t % 2));
+  };
+
+  StepCursor<G> c;
+  c.init(p);
+  int n = -1;
+  if constexpr (KV) {
+    for (int t = 0; c.valid(); ++t) {
+      const int nblk = c.nblk();
+      const bool first = c.s == 0;
+      const bool last = c.s == c.nsteps - 1;
+      c.advance(p);
+      if (first) {
+        ++n;
+        if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) break;
+      }
+      if (!mbar_wait(bar(C::kBarXF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) break;
+      // T1/T2 are free once the previous step's MMA3/MMA4 have read E1/E2 from them.
+      if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
+      tc_fence_after();
+      const uint32_t xs = x0 + (t % 2) * kStage, ys = y0 + (t % 2) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
+        const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
+        if (BLK == 128) {
+          tc_mma_ss_lh(t1, a0 + ia, hi, xs + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+          tc_mma_ss_lh(t2, b0 + ia, hi, ys + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            if (g < nblk) {
+              const uint32_t go = (g * C::kBlkB) >> 4;
+              tc_mma_ss_lh(t1 + g * BLK, a0 + ia, hi, xs + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
+              tc_mma_ss_lh(t2 + g * BLK, b0 + ia, hi, ys + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
+            }
+        }
+      }
+      tc_commit(bar(C::kBarTF));
+      if (last) tc_commit(bar(C::kBarIE));
+      if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
+      // An item's first accumulation overwrites the accumulators: the previous item's must
+      // have been read out.
+      if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+      tc_fence_after();
+      const uint32_t xm = xm0 + (t % 2) * kStage, ym = ym0 + (t % 2) * kStage;
+      const int ksteps = nblk * BLK / 16;
+#pragma unroll
+      for (int kk = 0; kk < 128 / 16; ++kk) {
+        if (kk < ksteps) {
+          const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+          const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+          tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
+          tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
+        }
+      }
+      tc_commit(bar(C::kBarAD));
+      tc_commit(bar(C::kBarXE + t % 2));
+    }
+  } else {
+    // Step u's T1 region, and its accumulation once E1 (dS) is written: dQ += dS K.
+    auto t1_of = [&](int u) { return tmem + ((u & 1) ? C::kT1b : C::kT1); };
+    auto mma3 = [&](int u, int nb, bool fst, int item) -> bool {
+      // An item's first accumulation overwrites acc1: the previous item's must have been
+      // read out.
+      if (fst && item > 0 && !mbar_wait(bar(C::kBarAR), (item - 1) & 1, ctl, kSiteMmaPFull))
+        return false;
+      tc_fence_after();
+      issue_second(acc1, t1_of(u), xm0 + (u % 3) * kStage, nb, fst);
+      tc_commit(bar(C::kBarAD + (u & 1)));
+      tc_commit(bar(C::kBarXE + u % 3));
+      return true;
+    };
+    int t = 0;
+    bool ok = true;
+    int pnb = 0, pitem = -1;  // step t-1: block count, item
+    bool pfirst = false;
+    for (; c.valid(); ++t) {
+      const int nblk = c.nblk();
+      const bool first = c.s == 0;
+      const bool last = c.s == c.nsteps - 1;
+      c.advance(p);
+      if (first) {
+        ++n;
+        if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+      }
+      if (!mbar_wait(bar(C::kBarXF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+      // This T1 region held step t-2, whose MMA3 read E1 from it (AD of that region cannot
+      // be a phase ahead: its next phase is step t's own MMA3).
+      if (t >= 2 && !mbar_wait(bar(C::kBarAD + (t & 1)), ((t - 2) / 2) & 1, ctl, kSiteMmaPvDone)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_first(t1_of(t), a0, x0 + (t % 3) * kStage, nblk);  // S = Q K^T
+      // T2 is free, and E1 of step t-1 written, once the elementwise warps finished it.
+      if (t >= 1 && !mbar_wait(bar(C::kBarEF), (t - 1) & 1, ctl, kSiteMmaPFull)) { ok = false; break; }
+      if (!mbar_wait(bar(C::kBarYF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+      tc_fence_after();
+      issue_first(t2, b0, y0 + (t % 2) * kStage, nblk);  // dP = dO V^T
+      tc_commit(bar(C::kBarTF));
+      tc_commit(bar(C::kBarYE + t % 2));
+      if (last) tc_commit(bar(C::kBarIE));
+      if (t >= 1 && !mma3(t - 1, pnb, pfirst, pitem)) { ok = false; break; }
+      pnb = nblk;
+      pfirst = first;
+      pitem = n;
+    }
+    if (ok && t >= 1) {
+      if (mbar_wait(bar(C::kBarEF), (t - 1) & 1, ctl, kSiteMmaPFull)) mma3(t - 1, pnb, pfirst, pitem);
+    }
   }
   tc_commit(bar(C::kBarDrain));
   mbar_drain_wait(bar(C::kBarDrain), 0);
@@ -283,9 +403,25 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
     return w;
   };
 
+  // dQ mode: the accumulator of the previous item, read out at the next item's first
+  // step once that step's E1 is handed over (its last MMA3 goes in only after that
+  // step's MMA2).
+  bool pending = false;
+  int prow = 0, pg = 0;  // its output row and last step
+  auto read_pending = [&]() -> bool {
+    if (!wait_bar(C::kBarAD + (pg & 1), (pg / 2) & 1, kSiteSoftItemDone)) return false;
+    uint32_t pk[D / 4];
+    read_o<D>(tl + C::kAcc1, p.scale, pk);
+    warp_arrive(C::kBarAR);
+    store_row_bf16<D>(p.out1, prow, half, pk);
+    pending = false;
+    return true;
+  };
+
   int g = 0;
+  bool ok = true;
   ItemStream is;
-  for (is.init<false>(p); !is.done(); is.next<false>(p)) {
+  for (is.init<false>(p); ok && !is.done(); is.next<false>(p)) {
     const int cnt = is.nnz();
     const int orow = is.cur.x * p.L + is.cur.y * BLK + row;  // this thread's output row
     if (cnt == 0) {
@@ -300,7 +436,6 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
     }
     const int dpos = p.causal_diag ? is.dpos() : -1;
     const int nsteps = (cnt + G - 1) / G;
-    bool ok = true;
     for (int s = 0; s < nsteps; ++s, ++g) {
       const int nblk = step_blocks<G>(cnt, s);
       const bool valid = (BLK == 128) || (half < nblk);
@@ -309,9 +444,10 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
         ok = false;
         break;
       }
+      const uint32_t t1 = tl + ((!KV && (g & 1)) ? C::kT1b : C::kT1);
       uint32_t rs[64], rp[64];
-      tmem_ld_16x32bx2_x32<64>(tl + C::kT1, *reinterpret_cast<uint32_t(*)[32]>(rs));
-      tmem_ld_16x32bx2_x32<64>(tl + C::kT1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+      tmem_ld_16x32bx2_x32<64>(t1, *reinterpret_cast<uint32_t(*)[32]>(rs));
+      tmem_ld_16x32bx2_x32<64>(t1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
       tmem_ld_16x32bx2_x32<64>(tl + C::kT2, *reinterpret_cast<uint32_t(*)[32]>(rp));
       tmem_ld_16x32bx2_x32<64>(tl + C::kT2 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
       tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs));
@@ -342,27 +478,32 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
         pk1[i] = pack_bf16x2(KV ? e[0] : ds[0], KV ? e[1] : ds[1]);
         pk2[i] = pack_bf16x2(ds[0], ds[1]);
       }
-      tmem_st_16x32bx2_x32<32>(tl + C::kT1, pk1);
+      tmem_st_16x32bx2_x32<32>(t1, pk1);
       if constexpr (KV) tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
       tmem_st_wait();
       warp_arrive(C::kBarEF);
+      if (!KV && s == 0 && pending && !read_pending()) {
+        ok = false;
+        break;
+      }
     }
     if (!ok) break;
-    // The item's accumulators are complete once its last step's MMA3/MMA4 are.
-    if (!wait_bar(C::kBarAD, (g - 1) & 1, kSiteSoftItemDone)) break;
-    uint32_t pk[D / 4];
-    read_o<D>(tl + C::kAcc1, KV ? 1.f : p.scale, pk);
     if constexpr (KV) {
-      uint32_t pk2[D / 4];
+      // The item's accumulators are complete once its last step's MMA3/MMA4 are.
+      if (!wait_bar(C::kBarAD, (g - 1) & 1, kSiteSoftItemDone)) break;
+      uint32_t pk[D / 4], pk2[D / 4];
+      read_o<D>(tl + C::kAcc1, 1.f, pk);
       read_o<D>(tl + C::kAcc2, p.scale, pk2);
       warp_arrive(C::kBarAR);
       store_row_bf16<D>(p.out1, orow, half, pk);
       store_row_bf16<D>(p.out2, orow, half, pk2);
     } else {
-      warp_arrive(C::kBarAR);
-      store_row_bf16<D>(p.out1, orow, half, pk);
+      pending = true;
+      prow = orow;
+      pg = g - 1;
     }
   }
+  if (!KV && ok && pending) read_pending();
 }
 
 // ------------------------------------------------------------------- kernel

@@ -39,10 +39,6 @@ constexpr int kMaxGrid = 1023;
 //   then the per-CTA starts (grid + 1 words) and col_idx (nnz words)
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchWords];
 
-// Device address of g_noalloc_scratch per device, looked up once with that device
-// current (host code must not use the symbol itself as a pointer).
-int32_t* g_scratch_addr[64] = {nullptr};
-
 size_t round4(size_t words) { return (words + 3) & ~static_cast<size_t>(3); }
 
 bool encode_rows_noalloc(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows,
@@ -93,13 +89,12 @@ extern "C" int bsa_forward_noalloc(const void* q, const void* k, const void* v, 
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BSA_ERR_CUDA;
-  if (g_scratch_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return BSA_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int32_t*>(ptr);
-  }
-  int32_t* base = g_scratch_addr[dev];
+  // Looked up on every call (it allocates nothing): a cached address would go stale if
+  // the device's context were reset and the module loaded again.
+  void* scratch = nullptr;
+  if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+    return BSA_ERR_CUDA;
+  int32_t* base = static_cast<int32_t*>(scratch);
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return BSA_ERR_CUDA;

@@ -319,9 +319,9 @@ int bsa_topk_forward(const void* q, const void* kv, const float* sink, const int
  * Limit: 4 + 4*n_items + 1024 + nnz int32 words (each part rounded up to 4 words) must
  * fit in 1 Mi words; larger LUTs return BSA_ERR_TOO_LARGE before
  * any device work.  The per-CTA schedule comes from bsa_lut_upload when the LUT was
- * uploaded on this device; otherwise the call builds it in host memory.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any
- * stream capture.  All calls share the array and each call overwrites it: calls
+ * uploaded on this device; otherwise the call builds it in host memory.  Each call
+ * looks up the array's device address (cudaGetSymbolAddress, which allocates nothing)
+ * on the current device.  All calls share the array and each call overwrites it: calls
  * whose kernels overlap on the GPU (other streams, other host threads) race, so
  * serialize them on one stream.  Other errors: as bsa_forward.
  */
