@@ -74,7 +74,12 @@ struct BwdCfg {
   static constexpr int kBarAD = 14;   // [2] a step's MMA3/MMA4 done (dQ mode: by T1 region)
   static constexpr int kBarAR = 16;   // accumulators read out (one arrive per elementwise warp)
   static constexpr int kBarDrain = 17;
-  static constexpr int kNumBars = 18;
+  static constexpr int kBarEF1 = 18;  // kSplitE: E1 (P^T) written (per elementwise warp)
+  static constexpr int kNumBars = 19;
+  // dK/dV mode at b = 64: P^T is handed over before dS^T is formed, so dV's MMAs overlap
+  // that pass (+4 % on a b = 64 workload; at b = 128 the extra live registers spill and
+  // it measured 1 % slower).
+  static constexpr bool kSplitE = KV && BLK == 64;
   static constexpr int kBarBytes = 192;  // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
@@ -296,20 +301,28 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
       }
       tc_commit(bar(C::kBarTF));
       if (last) tc_commit(bar(C::kBarIE));
-      if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
-      // An item's first accumulation overwrites the accumulators: the previous item's must
-      // have been read out.
+      // E1 (P^T) and E2 (dS^T) written; with kSplitE, dV's MMAs go in once P^T is and
+      // run while the warps form dS^T.  An item's first accumulation overwrites the
+      // accumulators: the previous item's must have been read out.
+      if (!mbar_wait(bar(C::kSplitE ? C::kBarEF1 : C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
       if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
       tc_fence_after();
       const uint32_t xm = xm0 + (t % 2) * kStage, ym = ym0 + (t % 2) * kStage;
-      const int ksteps = nblk * BLK / 16;
+      if constexpr (C::kSplitE) {
+        issue_second(acc1, t1, ym, nblk, first);  // dV += P^T dO
+        if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
+        tc_fence_after();
+        issue_second(acc2, t2, xm, nblk, first);  // dK += dS^T Q
+      } else {
+        const int ksteps = nblk * BLK / 16;
 #pragma unroll
-      for (int kk = 0; kk < 128 / 16; ++kk) {
-        if (kk < ksteps) {
-          const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-          const uint32_t accum = (first && kk == 0) ? 0u : 1u;
-          tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
-          tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          if (kk < ksteps) {
+            const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+            const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+            tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
+            tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
+          }
         }
       }
       tc_commit(bar(C::kBarAD));
@@ -458,28 +471,59 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
       // the query; dK/dV: query before the key).
       const int lo = (KV && diag) ? row - kbase : -(1 << 30);
       const int hi = (!KV && diag) ? row - kbase : (1 << 30);
-      uint32_t pk1[32], pk2[32];
       const float* vl = vec + (g % 2) * 256 + 64 * half;  // KV: this half's lse ...
       const float* vd = vl + 128;                         // ... and delta
+      if constexpr (C::kSplitE) {
+        // P^T first, handed over on its own so that dV's MMAs run while dS^T is formed;
+        // rs keeps P^T for the second pass.
+        uint32_t pk1[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float e[2], ds[2];
+        for (int i = 0; i < 32; ++i) {
+          float e[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cc = 2 * i + u;
-          const float l2 = KV ? vl[cc] * kLog2e : lr;
-          const float dd = KV ? vd[cc] : dr;
-          // masked after scaling, so that a negative scale cannot turn -inf into +inf
-          const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - l2, cc, lo, hi);
-          const float pe = valid ? ex2_approx(y) : 0.f;
-          e[u] = pe;
-          ds[u] = valid ? pe * (__uint_as_float(rp[cc]) - dd) : 0.f;
+          for (int u = 0; u < 2; ++u) {
+            const int cc = 2 * i + u;
+            // masked after scaling, so that a negative scale cannot turn -inf into +inf
+            const float y =
+                mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - vl[cc] * kLog2e, cc, lo, hi);
+            e[u] = valid ? ex2_approx(y) : 0.f;
+            rs[cc] = __float_as_uint(e[u]);
+          }
+          pk1[i] = pack_bf16x2(e[0], e[1]);
         }
-        pk1[i] = pack_bf16x2(KV ? e[0] : ds[0], KV ? e[1] : ds[1]);
-        pk2[i] = pack_bf16x2(ds[0], ds[1]);
+        tmem_st_16x32bx2_x32<32>(t1, pk1);
+        tmem_st_wait();
+        warp_arrive(C::kBarEF1);
+        uint32_t pk2[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c0 = 2 * i, c1 = 2 * i + 1;
+          pk2[i] = pack_bf16x2(__uint_as_float(rs[c0]) * (__uint_as_float(rp[c0]) - vd[c0]),
+                               __uint_as_float(rs[c1]) * (__uint_as_float(rp[c1]) - vd[c1]));
+        }
+        tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
+      } else {
+        uint32_t pk1[32], pk2[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float e[2], ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cc = 2 * i + u;
+            const float l2 = KV ? vl[cc] * kLog2e : lr;
+            const float dd = KV ? vd[cc] : dr;
+            // masked after scaling, so that a negative scale cannot turn -inf into +inf
+            const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - l2, cc, lo, hi);
+            const float pe = valid ? ex2_approx(y) : 0.f;
+            e[u] = pe;
+            ds[u] = valid ? pe * (__uint_as_float(rp[cc]) - dd) : 0.f;
+          }
+          pk1[i] = pack_bf16x2(KV ? e[0] : ds[0], KV ? e[1] : ds[1]);
+          pk2[i] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st_16x32bx2_x32<32>(t1, pk1);
+        if constexpr (KV) tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
       }
-      tmem_st_16x32bx2_x32<32>(t1, pk1);
-      if constexpr (KV) tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
       tmem_st_wait();
       warp_arrive(C::kBarEF);
       if (!KV && s == 0 && pending && !read_pending()) {
@@ -526,7 +570,7 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarEF || i == C::kBarAR) ? C::kEwWarps : 1);
+      mbar_init(bar(i), (i == C::kBarEF || i == C::kBarAR || i == C::kBarEF1) ? C::kEwWarps : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
