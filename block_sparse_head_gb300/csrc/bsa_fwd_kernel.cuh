@@ -39,15 +39,18 @@
 //               by three-input maxima and one shuffle, exp2(s*c - m) with the scale c =
 //               scale*log2(e) folded into a packed f32x2 FFMA), lazy rescale (the
 //               running max moves only when it grows by more than 2^8), P -> TMEM as bf16
-//               pairs over the S columns.  When an item ends, each row's (m, l) goes to
-//               the epilogue through shared memory; the softmax moves straight on.
-//   epilogue    the last warpgroup.  Per item: waits for the row statistics and the
-//               item's last PV, reads O out of TMEM (32x32b: one row per thread),
-//               releases the accumulator to the PV issuer, then stores O / l as bf16 and
-//               lse = ln 2 * (m + log2 l).  An item with no active block gets O = 0 and
-//               lse = -inf.
+//               pairs over the S columns.  When an item ends (b = 128), each row's
+//               (m, l) goes to the epilogue through shared memory and the softmax moves
+//               straight on; at b = 64 the softmax itself reads the item's O out at the
+//               next item's first step and stores it.
+//   epilogue    b = 128: the last warpgroup.  Per item: waits for the row statistics and
+//               the item's last PV, reads O out of TMEM (32x32b: one row per thread),
+//               releases the accumulator to the PV issuer, then stores O / l as bf16
+//               (32-byte stores spaced apart) and lse = ln 2 * (m + log2 l).
+//   An item with no active block gets O = 0 and lse = -inf (or the sink, EXT).
 //   At b = 128 the 16 warps are launched at 128 registers each and re-split per
-//   warpgroup with setmaxnreg (control 72, softmax 160, epilogue 120).
+//   warpgroup with setmaxnreg (control 72, softmax 160, epilogue 120); b = 64 runs the
+//   control warpgroup and one softmax warpgroup.
 // Work-list records (which carry each item's block indices, CSR row start and diagonal
 // position) are fetched two items ahead and column indices one step ahead of use, so no
 // role waits on a global load in its steady state.
