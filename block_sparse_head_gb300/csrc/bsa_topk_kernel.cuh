@@ -52,7 +52,8 @@ struct TopkCfg {
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffP = kOffKV + kKVBytes;
   static constexpr int kOffRed = kOffP + kPBytes;     // [4][64] partials, m[64], alpha[64],
-  static constexpr int kRedBytes = 2048;              // inv[64], flag
+  static constexpr int kRedBytes = 2048;              // inv[64], flag, vote
+  static constexpr int kVoteWord = 4 * 64 + 3 * 64 + 1;  // int index of the vote counter
   static constexpr int kOffBar = kOffRed + kRedBytes;
   static constexpr int kBarQF = 0, kBarQE = 1, kBarKF = 2 /* [4] */, kBarKE = 6 /* [4] */,
                        kBarSF = 10, kBarPF = 11, kBarPVD = 12, kBarOR = 13, kBarDrain = 14,
@@ -195,6 +196,8 @@ __device__ __forceinline__ void topk_softmax(const TopkParams& p, uint32_t sbase
   float* salpha = smax + 64;                                 // [64] rescale factors
   float* sinv = salpha + 64;                                 // [64] 1 / normaliser
   int* sflag = reinterpret_cast<int*>(sinv + 64);
+  int* svote = reinterpret_cast<int*>(red) + C::kVoteWord;  // latest step + 1 whose vote said
+                                                            // a max moves
   uint8_t* pt = smem + C::kOffP;
   const int nsteps = (p.K + C::kRows - 1) / C::kRows;
   auto wait = [&](int b, int parity, int site) {
@@ -301,40 +304,58 @@ __device__ __forceinline__ void topk_softmax(const TopkParams& p, uint32_t sbase
           x[32 + c] = valid ? __uint_as_float(r1[c]) * p.scale_log2 : -INFINITY;
         }
       }
-      // Per-head maximum over the step's 128 rows.
-      {
-        float v2[64];
+      // A head's running max moves only on a position's first step or when one of the
+      // step's scores exceeds it by more than 2^8 (log2 units).  Past the first step,
+      // whether any score does is a CTA-wide vote (one meeting); only then are the
+      // per-head maxima reduced (two more).  Every warp reads the vote before it
+      // gathers the next step's rows, and no warp votes on the next step before that
+      // step's S^T, which needs those rows: so the counter cannot have moved on when read.
+      bool full = (s == 0);
+      if (!full) {
+        bool need = false;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) v2[c] = x[c];
-        const float2 m2 = warp_reduce_scatter64<true>(v2);
-        reinterpret_cast<float2*>(red + 64 * qd)[lane] = m2;
+        for (int c = 0; c < 64; ++c) need |= x[c] > smax[c] + 8.f;
+        if (__any_sync(0xffffffffu, need) && lane == 0) atomicMax(svote, t + 1);
+        if (!group_sync()) { ok = false; break; }
+        full = *reinterpret_cast<volatile int*>(svote) >= t + 1;
       }
-      if (!group_sync()) { ok = false; break; }
-      if (qd == 0) {
-        // Lazy update: a head's running max moves only when it grows by more than 2^8
-        // (or on the position's first step); alpha rescales what was summed before.
-        bool moved = false;
+      bool moved = false;
+      if (full) {
+        // Per-head maximum over the step's 128 rows.
+        {
+          float v2[64];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = 2 * lane + u;
-          const float cm = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
-          const float old = smax[c];
-          float nw = old, a = 1.f;
-          if (s == 0) {
-            nw = cm;
-          } else if (cm > old + 8.f) {
-            nw = cm;
-            a = ex2_approx(old - cm);  // old = -inf gives 0
-            moved = true;
-          }
-          smax[c] = nw;
-          salpha[c] = a;
+          for (int c = 0; c < 64; ++c) v2[c] = x[c];
+          const float2 m2 = warp_reduce_scatter64<true>(v2);
+          reinterpret_cast<float2*>(red + 64 * qd)[lane] = m2;
         }
-        moved = __any_sync(0xffffffffu, moved);
-        if (lane == 0) *sflag = moved ? 1 : 0;
+        if (!group_sync()) { ok = false; break; }
+        if (qd == 0) {
+          // Lazy update: a head's running max moves only when it grows by more than 2^8
+          // (or on the position's first step); alpha rescales what was summed before.
+          bool mv = false;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 2 * lane + u;
+            const float cm = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
+            const float old = smax[c];
+            float nw = old, a = 1.f;
+            if (s == 0) {
+              nw = cm;
+            } else if (cm > old + 8.f) {
+              nw = cm;
+              a = ex2_approx(old - cm);  // old = -inf gives 0
+              mv = true;
+            }
+            smax[c] = nw;
+            salpha[c] = a;
+          }
+          mv = __any_sync(0xffffffffu, mv);
+          if (lane == 0) *sflag = mv ? 1 : 0;
+        }
+        if (!group_sync()) { ok = false; break; }
+        moved = *reinterpret_cast<volatile int*>(sflag) != 0;
       }
-      if (!group_sync()) { ok = false; break; }
-      const bool moved = *reinterpret_cast<volatile int*>(sflag) != 0;
       // P^T row (bf16, this row's 64 heads) into shared memory, 128-byte swizzle.
       uint32_t pk[32];
 #pragma unroll
@@ -451,6 +472,7 @@ __global__ void __launch_bounds__(TopkCfg::kThreads, 1)
       mbar_init(bar(i), (i == C::kBarPF || i == C::kBarOR || i == C::kBarG0 || i == C::kBarG1 ||
                        (i >= C::kBarKF && i < C::kBarKF + 4)) ? 4 : 1);
     *abort_flag = 0;
+    reinterpret_cast<int*>(smem + C::kOffRed)[C::kVoteWord] = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_q);
