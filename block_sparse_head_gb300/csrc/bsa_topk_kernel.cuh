@@ -15,7 +15,9 @@
 // S^T uses 64 TMEM columns and O^T 256.  The softmax then runs down the TMEM lanes (one
 // lane per gathered row): its per-head maximum and sum are reductions across the 128
 // lanes (a shuffle reduce-scatter within each warp, then shared memory across the four
-// warps).  P^T goes to shared memory as bf16, the B operand of the second product.
+// warps).  The running maximum moves lazily, so past a position's first step a CTA-wide
+// vote first decides whether any head's maximum moves at all, and only then is it
+// reduced.  P^T goes to shared memory as bf16, the B operand of the second product.
 // One CTA per SM walks positions m = blockIdx.x, blockIdx.x + gridDim.x, ...:
 //   warp 0      producer: the position's Q (one 3-D TMA copy, 64 KB).
 //   warp 1      MMA issuer (one thread) and TMEM owner.
