@@ -238,3 +238,47 @@ def test_forward_ext_validation(lib):
     assert call(ext=binding.ExtArgs(-1, -1, -1.0, None, None, None)) == -6  # negative softcap
     assert call(Lk=400) == -2 and call(Lq=500) == -2           # layout / length mismatch
     assert call() == -9                                        # valid, but never uploaded
+
+
+def test_backward_validation_before_device_work(lib):
+    """Argument errors of bsa_backward come back before any device work (fake pointers,
+    16-byte aligned, never dereferenced)."""
+    lut = bsa.build_lut(np.ones((2, 4, 4), np.int32), 1, upload=False)
+    A = 1 << 20
+
+    def f(**kw):
+        ptrs = [kw.get(n, A) for n in ("q", "k", "v", "out", "lse", "dout")]
+        outs = [kw.get(n, A) for n in ("dq", "dk", "dv", "delta")]
+        return lib.bsa_backward(*ptrs, kw.get("lut", lut.handle), *outs, kw.get("B", 1),
+                                kw.get("H", 2), kw.get("L", 256), kw.get("d", 64),
+                                ctypes.c_float(kw.get("scale", 0.125)), kw.get("block", 64),
+                                kw.get("causal", 1), None)
+
+    for name in ("q", "k", "v", "out", "lse", "dout", "lut", "dq", "dk", "dv", "delta"):
+        assert f(**{name: None}) == -1, name
+    assert f(block=32) == -6 and f(d=96) == -6 and f(scale=float("inf")) == -6
+    assert f(B=2) == -2 and f(H=3) == -2 and f(L=512) == -2 and f(L=0) == -2
+    for name in ("q", "dout", "dq", "delta"):
+        assert f(**{name: A + 4}) == -5, name
+    assert f() == -9  # valid arguments, but the LUT was never uploaded
+
+
+def test_topk_validation_before_device_work(lib):
+    """Argument errors of bsa_topk_forward come back before any device work."""
+    A = 1 << 20
+
+    def f(**kw):
+        return lib.bsa_topk_forward(
+            kw.get("q", A), kw.get("kv", A), kw.get("sink", A), kw.get("idx", A),
+            kw.get("out", A), kw.get("lse", A), kw.get("status", A), kw.get("B", 1),
+            kw.get("M", 16), kw.get("N", 256), kw.get("H", 64), kw.get("D", 512),
+            kw.get("K", 128), ctypes.c_float(kw.get("scale", 0.05)), None)
+
+    for name in ("q", "kv", "sink", "idx", "out", "lse", "status"):
+        assert f(**{name: None}) == -1, name
+    assert f(H=32) == -6 and f(D=256) == -6 and f(scale=float("nan")) == -6
+    assert f(B=0) == -2 and f(M=0) == -2 and f(N=0) == -2 and f(K=0) == -2
+    assert f(M=1 << 20, B=64) == -2  # B * M * H past the int32 range
+    for name in ("q", "kv", "idx", "out", "lse"):
+        assert f(**{name: A + 8}) == -5, name
+    assert f(status=A + 2) == -5
