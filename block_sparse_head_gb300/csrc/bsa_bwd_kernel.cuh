@@ -26,10 +26,14 @@
 //   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2..   elementwise warpgroups (two at b = 128, one at b = 64), laid out as the
 //               forward's softmax: per step they read T1 and T2, form P and dS, and write
-//               the bf16 operands E1 (over T1) and E2 (over T2) for the second MMAs.  At an
-//               item's end they read the accumulators, scale and store them as bf16.
-// dK/dV mode: T1 (128 columns), T2 (128), acc1 and acc2 (d each) fill the 512 columns, so
-// each step runs MMA1/MMA2 -> elementwise -> MMA3/MMA4 in order.
+//               the bf16 operands for the second MMAs into TMEM.  At an item's end they
+//               read the accumulators, scale and store them as bf16.
+// dK/dV mode: T1 and T2 (128 columns each) and acc1 and acc2 (d each) fill the 512
+// columns.  E1 and E2 (bf16, 64 columns each) both go over T1, so T2 is free as soon as
+// the warps have loaded it and takes the next step's T1: the regions swap every step.
+// MMA1 of step t+1 then runs while the warps form E2 of step t, and MMA2 of step t+1 (into
+// the region E1/E2 of step t leave) follows MMA3/MMA4 of step t.  The item tile B gets a
+// barrier of its own, so that A reloads once the item's last MMA1 is done.
 // dQ mode: T1 alternates between two 128-column regions (steps of even and odd index)
 // beside T2 and acc1.  MMA1 of step t goes in as soon as MMA3 of step t-2 has read its
 // region, so it runs while the elementwise warps work on step t-1; MMA3 of step t-1 goes in
@@ -69,24 +73,26 @@ struct BwdCfg {
   static constexpr int kBarXE = 5;    // [kNX] X free (its step's MMA3 (and MMA4) done)
   static constexpr int kBarYF = 8;    // [2] dQ mode: Y landed
   static constexpr int kBarYE = 10;   // [2] dQ mode: Y free (its step's MMA2 done)
-  static constexpr int kBarTF = 12;   // T1, T2 computed
+  static constexpr int kBarTF = 12;   // T1, T2 computed (dK/dV mode: T1 = S^T only)
   static constexpr int kBarEF = 13;   // E1 (E2) written (one arrive per elementwise warp)
   static constexpr int kBarAD = 14;   // [2] a step's MMA3/MMA4 done (dQ mode: by T1 region)
   static constexpr int kBarAR = 16;   // accumulators read out (one arrive per elementwise warp)
   static constexpr int kBarDrain = 17;
-  static constexpr int kBarEF1 = 18;  // kSplitE: E1 (P^T) written (per elementwise warp)
-  static constexpr int kNumBars = 19;
-  // dK/dV mode at b = 64: P^T is handed over before dS^T is formed, so dV's MMAs overlap
-  // that pass (+4 % on a b = 64 workload; at b = 128 the extra live registers spill and
-  // it measured 1 % slower).
-  static constexpr bool kSplitE = KV && BLK == 64;
+  static constexpr int kBarEF1 = 18;  // dK/dV mode: E1 (P^T) written (per elementwise warp)
+  static constexpr int kBarDF = 19;   // dK/dV mode: T2 (dP^T) computed
+  static constexpr int kBarDL = 20;   // dK/dV mode: T2 loaded by every elementwise warp
+  static constexpr int kBarIFV = 21;  // dK/dV mode: item tile B (V) landed; kBarIF is A's
+  static constexpr int kBarIEV = 22;  // dK/dV mode: item tile B free; kBarIE is A's
+  static constexpr int kNumBars = 23;
   static constexpr int kBarBytes = 192;  // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr int kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
   // TMEM columns.  dQ mode: T1 at 0 (even steps) or 256 (odd steps), T2 at 128, acc1 at
-  // 384.  dK/dV mode: T1 at 0, T2 at 128, acc1 at 256, acc2 after it.
+  // 384.  dK/dV mode: T1 and T2 swap between the regions at 0 and 128 from one step to
+  // the next (T1 at 0 on even steps), E1 and E2 (bf16) share T1's region; acc1 at 256,
+  // acc2 after it.
   static constexpr int kT1 = 0, kT2 = 128, kT1b = 256;
   static constexpr int kAcc1 = KV ? 256 : 384, kAcc2 = 256 + D;
   static_assert(KV ? (kAcc2 + D <= 512) : (kAcc1 + D <= 512), "TMEM budget");
@@ -130,6 +136,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
   c.init(p);
   int n = -1, t = 0;
   int nx = 0, ny = 0;  // dQ mode: steps whose X (Y) copies were armed
+  int nv = 0;          // dK/dV mode: items whose B was armed
   bool ok = true;
   for (; c.valid(); ++t) {
     const int nblk = c.nblk();
@@ -137,19 +144,21 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
     int cols[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) cols[g] = (g < nblk) ? p.col_idx[c.is.cur.z + c.s * G + g] : 0;
-    if (c.s == 0) {
-      // Item tiles: one buffer, free once the previous item's last MMA1/MMA2 completed.
-      // n counts the items whose tiles were armed.
+    const bool item_first = c.s == 0;
+    const int irow = bh * p.L + c.is.cur.y * BLK;  // the item's first row
+    if (item_first) {
+      // Item tiles: one buffer each.  A is free once the previous item's last MMA1
+      // completed; dQ mode loads B with it (free once that item's last MMA2 completed).
+      // n counts the items whose A was armed.
       if (n >= 0 && !mbar_wait(bar(C::kBarIE), n & 1, ctl, kSiteProdKEmpty)) {
         ok = false;
         break;
       }
       const uint32_t fb = bar(C::kBarIF);
-      mbar_arrive_expect_tx(fb, 2 * C::kItemTile);
+      mbar_arrive_expect_tx(fb, (KV ? 1 : 2) * C::kItemTile);
       ++n;
-      const int row = bh * p.L + c.is.cur.y * BLK;
-      tma_load_3d(sbase + C::kOffA, tm_a, fb, 0, row, 0);
-      tma_load_3d(sbase + C::kOffB, tm_b, fb, 0, row, 0);
+      tma_load_3d(sbase + C::kOffA, tm_a, fb, 0, irow, 0);
+      if constexpr (!KV) tma_load_3d(sbase + C::kOffB, tm_b, fb, 0, irow, 0);
     }
     c.advance(p);
     if constexpr (KV) {
@@ -172,6 +181,18 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
           bulk_load(vd, p.lse + row, BLK * 4, fb);
           bulk_load(vd + 512, p.delta + row, BLK * 4, fb);
         }
+      }
+      if (item_first) {
+        // B (V) after the step's tiles: the previous item's last MMA2, which frees its
+        // slot, goes in after that item's last MMA1 and completes later.
+        if (nv > 0 && !mbar_wait(bar(C::kBarIEV), (nv - 1) & 1, ctl, kSiteProdKEmpty)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fv = bar(C::kBarIFV);
+        mbar_arrive_expect_tx(fv, C::kItemTile);
+        tma_load_3d(sbase + C::kOffB, tm_b, fv, 0, irow, 0);
+        ++nv;
       }
     } else {
       // X slot t % 3 held K(t-3), read by MMA3(t-3); Y slot t % 2 held V(t-2), read by
@@ -209,6 +230,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
   }
   (void)ok;
   if (n >= 0) mbar_drain_wait(bar(C::kBarIF), n & 1);
+  if (KV && nv > 0) mbar_drain_wait(bar(C::kBarIFV), (nv - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -232,7 +254,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   const uint32_t xm0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffX, C::kHalf, 1024));
   const uint32_t ym0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, C::kHalf, 1024));
   constexpr uint32_t kStage = C::kStepTile >> 4;
-  const uint32_t t1 = tmem + C::kT1, t2 = tmem + C::kT2;
+  const uint32_t t2 = tmem + C::kT2;
   const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
   // T = item tile (A or B) x step tile^T over d: one N = 128 MMA per 16 columns of d, or
   // one N = 64 MMA per block at b = 64.
@@ -268,65 +290,72 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   c.init(p);
   int n = -1;
   if constexpr (KV) {
-    for (int t = 0; c.valid(); ++t) {
-      const int nblk = c.nblk();
-      const bool first = c.s == 0;
-      const bool last = c.s == c.nsteps - 1;
+    // T1(t) (S^T, then E1 = P^T in its first 64 columns and E2 = dS^T in the next 64) is
+    // the region at 0 on even steps and at 128 on odd ones; T2(t) (dP^T) is the other.
+    // Per step t:
+    //   MMA2(t) into T2(t) = T1(t-1), once MMA3/MMA4(t-1) have read E1/E2 there;
+    //   MMA3(t) (dV += P^T dO) once E1 is written;
+    //   MMA1(t+1) into T1(t+1) = T2(t), once every elementwise warp has loaded dP^T(t);
+    //   MMA4(t) (dK += dS^T Q) once E2 is written.
+    // So MMA3(t) and MMA1(t+1) run while the warps form dS^T(t), and MMA4(t) and
+    // MMA2(t+1) while they form P^T(t+1).
+    auto reg1 = [&](int t) { return tmem + ((t & 1) ? C::kT2 : C::kT1); };
+    auto reg2 = [&](int t) { return tmem + ((t & 1) ? C::kT1 : C::kT2); };
+    if (c.valid()) {
+      int nblk = c.nblk();
+      bool first = true;
+      bool last = c.s == c.nsteps - 1;
       c.advance(p);
-      if (first) {
-        ++n;
-        if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) break;
+      n = 0;
+      bool ok = mbar_wait(bar(C::kBarIF), 0, ctl, kSiteMmaStage) &&
+                mbar_wait(bar(C::kBarXF), 0, ctl, kSiteMmaStage);
+      if (ok) {
+        tc_fence_after();
+        issue_first(reg1(0), a0, x0, nblk);  // S^T = K Q^T
+        tc_commit(bar(C::kBarTF));
+        if (last) tc_commit(bar(C::kBarIE));
       }
-      if (!mbar_wait(bar(C::kBarXF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) break;
-      // T1/T2 are free once the previous step's MMA3/MMA4 have read E1/E2 from them.
-      if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
-      tc_fence_after();
-      const uint32_t xs = x0 + (t % 2) * kStage, ys = y0 + (t % 2) * kStage;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
-        const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
-        if (BLK == 128) {
-          tc_mma_ss_lh(t1, a0 + ia, hi, xs + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
-          tc_mma_ss_lh(t2, b0 + ia, hi, ys + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            if (g < nblk) {
-              const uint32_t go = (g * C::kBlkB) >> 4;
-              tc_mma_ss_lh(t1 + g * BLK, a0 + ia, hi, xs + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
-              tc_mma_ss_lh(t2 + g * BLK, b0 + ia, hi, ys + is + go, hi, C::kIdesc1b, kk > 0 ? 1u : 0u);
-            }
+      for (int t = 0; ok; ++t) {
+        const uint32_t st = (t % 2) * kStage;
+        if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
+        if (first && !mbar_wait(bar(C::kBarIFV), n & 1, ctl, kSiteMmaStage)) break;
+        tc_fence_after();
+        issue_first(reg2(t), b0, y0 + st, nblk);  // dP^T = V dO^T
+        tc_commit(bar(C::kBarDF));
+        if (last) tc_commit(bar(C::kBarIEV));
+        // An item's first accumulation overwrites the accumulators: the previous item's
+        // must have been read out.
+        if (!mbar_wait(bar(C::kBarEF1), t & 1, ctl, kSiteMmaPFull)) break;
+        if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+        tc_fence_after();
+        issue_second(acc1, reg1(t), ym0 + st, nblk, first);  // dV += P^T dO
+        const bool more = c.valid();
+        int nblk2 = 0;
+        bool first2 = false, last2 = false;
+        if (more) {
+          nblk2 = c.nblk();
+          first2 = c.s == 0;
+          last2 = c.s == c.nsteps - 1;
+          c.advance(p);
+          if (!mbar_wait(bar(C::kBarDL), t & 1, ctl, kSiteMmaPFull)) break;
+          if (first2 && !mbar_wait(bar(C::kBarIF), (n + 1) & 1, ctl, kSiteMmaStage)) break;
+          if (!mbar_wait(bar(C::kBarXF + (t + 1) % 2), ((t + 1) / 2) & 1, ctl, kSiteMmaStage)) break;
+          tc_fence_after();
+          issue_first(reg1(t + 1), a0, x0 + ((t + 1) % 2) * kStage, nblk2);
+          tc_commit(bar(C::kBarTF));
+          if (last2) tc_commit(bar(C::kBarIE));
         }
-      }
-      tc_commit(bar(C::kBarTF));
-      if (last) tc_commit(bar(C::kBarIE));
-      // E1 (P^T) and E2 (dS^T) written; with kSplitE, dV's MMAs go in once P^T is and
-      // run while the warps form dS^T.  An item's first accumulation overwrites the
-      // accumulators: the previous item's must have been read out.
-      if (!mbar_wait(bar(C::kSplitE ? C::kBarEF1 : C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
-      if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
-      tc_fence_after();
-      const uint32_t xm = xm0 + (t % 2) * kStage, ym = ym0 + (t % 2) * kStage;
-      if constexpr (C::kSplitE) {
-        issue_second(acc1, t1, ym, nblk, first);  // dV += P^T dO
         if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
         tc_fence_after();
-        issue_second(acc2, t2, xm, nblk, first);  // dK += dS^T Q
-      } else {
-        const int ksteps = nblk * BLK / 16;
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          if (kk < ksteps) {
-            const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-            const uint32_t accum = (first && kk == 0) ? 0u : 1u;
-            tc_mma_ts_lh(acc1, t1 + kk * 8, ym + bo, hi, C::kIdesc3, accum);  // dV += P^T dO
-            tc_mma_ts_lh(acc2, t2 + kk * 8, xm + bo, hi, C::kIdesc3, accum);  // dK += dS^T Q
-          }
-        }
+        issue_second(acc2, reg1(t) + 64, xm0 + st, nblk, first);  // dK += dS^T Q
+        tc_commit(bar(C::kBarAD));
+        tc_commit(bar(C::kBarXE + t % 2));
+        if (!more) break;
+        if (first2) ++n;
+        nblk = nblk2;
+        first = first2;
+        last = last2;
       }
-      tc_commit(bar(C::kBarAD));
-      tc_commit(bar(C::kBarXE + t % 2));
     }
   } else {
     // Step u's T1 region, and its accumulation once E1 (dS) is written: dQ += dS K.
@@ -453,30 +482,25 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
       const int nblk = step_blocks<G>(cnt, s);
       const bool valid = (BLK == 128) || (half < nblk);
       const bool diag = valid && (((BLK == 128) ? s : s * 2 + half) == dpos);
-      if (!wait_bar(C::kBarTF, g & 1, kSiteSoftSFull)) {
-        ok = false;
-        break;
-      }
-      const uint32_t t1 = tl + ((!KV && (g & 1)) ? C::kT1b : C::kT1);
-      uint32_t rs[64], rp[64];
-      tmem_ld_16x32bx2_x32<64>(t1, *reinterpret_cast<uint32_t(*)[32]>(rs));
-      tmem_ld_16x32bx2_x32<64>(t1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
-      tmem_ld_16x32bx2_x32<64>(tl + C::kT2, *reinterpret_cast<uint32_t(*)[32]>(rp));
-      tmem_ld_16x32bx2_x32<64>(tl + C::kT2 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs + 32));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp + 32));
-      // Masked columns: the diagonal block's entries above the diagonal (dQ: key after
-      // the query; dK/dV: query before the key).
-      const int lo = (KV && diag) ? row - kbase : -(1 << 30);
-      const int hi = (!KV && diag) ? row - kbase : (1 << 30);
-      const float* vl = vec + (g % 2) * 256 + 64 * half;  // KV: this half's lse ...
-      const float* vd = vl + 128;                         // ... and delta
-      if constexpr (C::kSplitE) {
-        // P^T first, handed over on its own so that dV's MMAs run while dS^T is formed;
-        // rs keeps P^T for the second pass.
-        uint32_t pk1[32];
+      if constexpr (KV) {
+        // T1 (S^T, then P^T | dS^T) and T2 (dP^T) swap regions every step.
+        const uint32_t t1 = tl + ((g & 1) ? C::kT2 : C::kT1);
+        const uint32_t t2 = tl + ((g & 1) ? C::kT1 : C::kT2);
+        const int lo = diag ? row - kbase : -(1 << 30);  // query before the key: masked
+        const float* vl = vec + (g % 2) * 256 + 64 * half;  // this half's lse ...
+        const float* vd = vl + 128;                         // ... and delta
+        if (!wait_bar(C::kBarTF, g & 1, kSiteSoftSFull)) {
+          ok = false;
+          break;
+        }
+        uint32_t rs[64];
+        tmem_ld_16x32bx2_x32<64>(t1, *reinterpret_cast<uint32_t(*)[32]>(rs));
+        tmem_ld_16x32bx2_x32<64>(t1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+        // P^T over the first 64 columns of T1, handed over on its own so that dV's MMAs
+        // run while dS^T is formed; rs keeps P^T (fp32) for dS^T.
+        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           float e[2];
@@ -484,51 +508,76 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
           for (int u = 0; u < 2; ++u) {
             const int cc = 2 * i + u;
             // masked after scaling, so that a negative scale cannot turn -inf into +inf
-            const float y =
-                mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - vl[cc] * kLog2e, cc, lo, hi);
+            const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - vl[cc] * kLog2e,
+                                         cc, lo, 1 << 30);
             e[u] = valid ? ex2_approx(y) : 0.f;
             rs[cc] = __float_as_uint(e[u]);
           }
-          pk1[i] = pack_bf16x2(e[0], e[1]);
+          pk[i] = pack_bf16x2(e[0], e[1]);
         }
-        tmem_st_16x32bx2_x32<32>(t1, pk1);
+        tmem_st_16x32bx2_x32<32>(t1, pk);
         tmem_st_wait();
         warp_arrive(C::kBarEF1);
-        uint32_t pk2[32];
+        if (!wait_bar(C::kBarDF, g & 1, kSiteSoftSFull)) {
+          ok = false;
+          break;
+        }
+        uint32_t rp[64];
+        tmem_ld_16x32bx2_x32<64>(t2, *reinterpret_cast<uint32_t(*)[32]>(rp));
+        tmem_ld_16x32bx2_x32<64>(t2 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+        warp_arrive(C::kBarDL);  // T2 may now take the next step's S^T
+        // dS^T over the next 64 columns of T1.
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c0 = 2 * i, c1 = 2 * i + 1;
-          pk2[i] = pack_bf16x2(__uint_as_float(rs[c0]) * (__uint_as_float(rp[c0]) - vd[c0]),
-                               __uint_as_float(rs[c1]) * (__uint_as_float(rp[c1]) - vd[c1]));
+          const float d0 = __uint_as_float(rs[c0]) * (__uint_as_float(rp[c0]) - vd[c0]);
+          const float d1 = __uint_as_float(rs[c1]) * (__uint_as_float(rp[c1]) - vd[c1]);
+          pk[i] = valid ? pack_bf16x2(d0, d1) : 0u;
         }
-        tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
+        tmem_st_16x32bx2_x32<32>(t1 + 64, pk);
+        tmem_st_wait();
+        warp_arrive(C::kBarEF);
       } else {
-        uint32_t pk1[32], pk2[32];
+        if (!wait_bar(C::kBarTF, g & 1, kSiteSoftSFull)) {
+          ok = false;
+          break;
+        }
+        const uint32_t t1 = tl + ((g & 1) ? C::kT1b : C::kT1);
+        uint32_t rs[64], rp[64];
+        tmem_ld_16x32bx2_x32<64>(t1, *reinterpret_cast<uint32_t(*)[32]>(rs));
+        tmem_ld_16x32bx2_x32<64>(t1 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+        tmem_ld_16x32bx2_x32<64>(tl + C::kT2, *reinterpret_cast<uint32_t(*)[32]>(rp));
+        tmem_ld_16x32bx2_x32<64>(tl + C::kT2 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+        // Masked columns: the diagonal block's entries above the diagonal (key after the
+        // query).
+        const int hi = diag ? row - kbase : (1 << 30);
+        uint32_t pk1[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float e[2], ds[2];
+          float ds[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int cc = 2 * i + u;
-            const float l2 = KV ? vl[cc] * kLog2e : lr;
-            const float dd = KV ? vd[cc] : dr;
             // masked after scaling, so that a negative scale cannot turn -inf into +inf
-            const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - l2, cc, lo, hi);
+            const float y = mask_outside(__uint_as_float(rs[cc]) * p.scale_log2 - lr, cc, -(1 << 30), hi);
             const float pe = valid ? ex2_approx(y) : 0.f;
-            e[u] = pe;
-            ds[u] = valid ? pe * (__uint_as_float(rp[cc]) - dd) : 0.f;
+            ds[u] = valid ? pe * (__uint_as_float(rp[cc]) - dr) : 0.f;
           }
-          pk1[i] = pack_bf16x2(KV ? e[0] : ds[0], KV ? e[1] : ds[1]);
-          pk2[i] = pack_bf16x2(ds[0], ds[1]);
+          pk1[i] = pack_bf16x2(ds[0], ds[1]);
         }
         tmem_st_16x32bx2_x32<32>(t1, pk1);
-        if constexpr (KV) tmem_st_16x32bx2_x32<32>(tl + C::kT2, pk2);
-      }
-      tmem_st_wait();
-      warp_arrive(C::kBarEF);
-      if (!KV && s == 0 && pending && !read_pending()) {
-        ok = false;
-        break;
+        tmem_st_wait();
+        warp_arrive(C::kBarEF);
+        if (s == 0 && pending && !read_pending()) {
+          ok = false;
+          break;
+        }
       }
     }
     if (!ok) break;
@@ -570,7 +619,9 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarEF || i == C::kBarAR || i == C::kBarEF1) ? C::kEwWarps : 1);
+      mbar_init(bar(i), (i == C::kBarEF || i == C::kBarAR || i == C::kBarEF1 || i == C::kBarDL)
+                           ? C::kEwWarps
+                           : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
