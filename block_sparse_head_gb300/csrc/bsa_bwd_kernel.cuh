@@ -63,8 +63,12 @@ struct BwdCfg {
   static constexpr int kOffB = kItemTile;
   static constexpr int kOffX = 2 * kItemTile;              // [kNX] slots
   static constexpr int kOffY = kOffX + kNX * kStepTile;    // [2] slots
-  static constexpr int kOffVec = kOffY + 2 * kStepTile;    // [2] stages x {lse, delta}[128] fp32
-  static constexpr int kVecBytes = KV ? 2 * 2 * 128 * 4 : 0;
+  // dK/dV mode, per stage: lse of the step's 128 query rows, then delta, fp32, each as two
+  // 64-row chunks 272 bytes apart (256 + 16), so that the two half-warps, which read
+  // different chunks with the same index, hit different banks.
+  static constexpr int kVecChunk = 272, kVecDelta = 2 * kVecChunk, kVecStage = 4 * kVecChunk;
+  static constexpr int kOffVec = kOffY + 2 * kStepTile;    // [2] stages
+  static constexpr int kVecBytes = KV ? 2 * kVecStage : 0;
   static constexpr int kOffBar = kOffVec + kVecBytes;
   // barriers
   static constexpr int kBarIF = 0;    // item tiles landed
@@ -177,9 +181,13 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const CUtensorM
           const int row = bh * p.L + cols[g] * BLK;
           tma_load_3d(xd + g * C::kBlkB, tm_x, fb, 0, row, 0);
           tma_load_3d(yd + g * C::kBlkB, tm_y, fb, 0, row, 0);
-          const uint32_t vd = sbase + C::kOffVec + (t % 2) * 1024 + g * BLK * 4;
-          bulk_load(vd, p.lse + row, BLK * 4, fb);
-          bulk_load(vd + 512, p.delta + row, BLK * 4, fb);
+#pragma unroll
+          for (int h = 0; h < BLK / 64; ++h) {
+            const uint32_t vd = sbase + C::kOffVec + (t % 2) * C::kVecStage +
+                                (g * (BLK / 64) + h) * C::kVecChunk;
+            bulk_load(vd, p.lse + row + 64 * h, 256, fb);
+            bulk_load(vd + C::kVecDelta, p.delta + row + 64 * h, 256, fb);
+          }
         }
       }
       if (item_first) {
@@ -258,31 +266,41 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
   // T = item tile (A or B) x step tile^T over d: one N = 128 MMA per 16 columns of d, or
   // one N = 64 MMA per block at b = 64.
+  // A branch between two MMAs slows their issue, so the block count of a step is tested
+  // once, not between MMAs.
   auto issue_first = [&](uint32_t td, uint32_t it, uint32_t st, int nblk) {
+    auto mmas = [&](int nb) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
-      const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
-      if (BLK == 128) {
-        tc_mma_ss_lh(td, it + ia, hi, st + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
-      } else {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ia = ((kk >> 2) * (BLK * 128) + (kk & 3) * 32) >> 4;  // item tile offset
+        const uint32_t is = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;     // step block offset
+        if (BLK == 128) {
+          tc_mma_ss_lh(td, it + ia, hi, st + is, hi, C::kIdesc1, kk > 0 ? 1u : 0u);
+        } else {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          if (g < nblk)
+          for (int g = 0; g < nb; ++g)
             tc_mma_ss_lh(td + g * BLK, it + ia, hi, st + is + ((g * C::kBlkB) >> 4), hi,
                          C::kIdesc1b, kk > 0 ? 1u : 0u);
+        }
       }
-    }
+    };
+    if (BLK == 64 && nblk > 1)
+      mmas(2);
+    else
+      mmas(1);
   };
-  // acc += E (bf16 in TMEM, 128 columns of the step) x step tile (MN-major).
+  // acc += E (bf16 in TMEM, 128 columns of the step) x step tile (MN-major); K = 16 rows
+  // of the step per MMA.
   auto issue_second = [&](uint32_t acc, uint32_t te, uint32_t sm, int nblk, bool first) {
-    const int ksteps = nblk * BLK / 16;
+    auto one = [&](int kk) {
+      const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+      tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
+    };
 #pragma unroll
-    for (int kk = 0; kk < 128 / 16; ++kk) {
-      if (kk < ksteps) {
-        const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-        tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
-      }
+    for (int kk = 0; kk < (BLK == 128 ? 8 : 4); ++kk) one(kk);
+    if (BLK == 64 && nblk > 1) {
+#pragma unroll
+      for (int kk = 4; kk < 8; ++kk) one(kk);
     }
   };
 
@@ -431,7 +449,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
   const int row = (BLK == 128) ? (wq * 32 + wg * 16 + (lane & 15)) : (wq * 16 + (lane & 15));
   const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32 + (BLK == 128 ? wg * 16 : 0)) << 16);
   const int kbase = (BLK == 128) ? 64 * half : 0;  // first column of this half in its block
-  const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec);  // KV: [stage][lse | delta][128]
+  const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec);  // KV: lse and delta
 
   auto warp_arrive = [&](int b) {
     tc_fence_before();
@@ -487,8 +505,8 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
         const uint32_t t1 = tl + ((g & 1) ? C::kT2 : C::kT1);
         const uint32_t t2 = tl + ((g & 1) ? C::kT1 : C::kT2);
         const int lo = diag ? row - kbase : -(1 << 30);  // query before the key: masked
-        const float* vl = vec + (g % 2) * 256 + 64 * half;  // this half's lse ...
-        const float* vd = vl + 128;                         // ... and delta
+        const float* vl = vec + ((g % 2) * C::kVecStage + half * C::kVecChunk) / 4;  // lse ...
+        const float* vd = vl + C::kVecDelta / 4;                                    // ... delta
         if (!wait_bar(C::kBarTF, g & 1, kSiteSoftSFull)) {
           ok = false;
           break;

@@ -376,21 +376,28 @@ __device__ __forceinline__ void fwd_mma_s(const FwdParams& p, uint32_t sbase, ui
     const uint32_t qlo = md.q0 + qb * (C::kQTile >> 4);
     const uint32_t klo = md.k0 + (t % 3) * kTileStep;
     // KB = 128: one N = 128 MMA per 16 columns of d.  KB = 64: one N = 64 MMA per block
-    // (the blocks' rows are not contiguous), into S columns [64g, 64g + 64).
+    // (the blocks' rows are not contiguous), into S columns [64g, 64g + 64), the two
+    // blocks' MMAs alternating.  The block count is tested once, not between MMAs (a
+    // branch between two MMAs slows their issue).
+    auto s_mmas = [&](int nb) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t qa = qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4);
-      const uint32_t kb = klo + (((kk >> 2) * C::kHalfB + (kk & 3) * 32) >> 4);
-      if (KB == 128) {
-        tc_mma_ss_lh(sb, qa, md.hi, kb, md.hi, C::kIdescS, kk > 0 ? 1u : 0u);
-      } else {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t qa = qlo + (((kk >> 2) * C::kQRegion + (kk & 3) * 32) >> 4);
+        const uint32_t kb = klo + (((kk >> 2) * C::kHalfB + (kk & 3) * 32) >> 4);
+        if (KB == 128) {
+          tc_mma_ss_lh(sb, qa, md.hi, kb, md.hi, C::kIdescS, kk > 0 ? 1u : 0u);
+        } else {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          if (g < nblk)
+          for (int g = 0; g < nb; ++g)
             tc_mma_ss_lh(sb + g * KB, qa, md.hi, kb + ((g * C::kBlkB) >> 4), md.hi, C::kIdescS1,
                          kk > 0 ? 1u : 0u);
+        }
       }
-    }
+    };
+    if (KB == 64 && nblk > 1)
+      s_mmas(2);
+    else
+      s_mmas(1);
     tc_commit(bar(C::kBarSF + t % 3));
   }
   // Let every MMA this thread issued finish before TMEM is released.
@@ -427,14 +434,21 @@ __device__ __forceinline__ void fwd_mma_pv(const FwdParams& p, uint32_t sbase, u
     const uint32_t ps = tmem + (g % 3) * 128;
     const uint32_t od = tmem + C::kOCol;
     const uint32_t vlo = md.v0 + (g % C::kNV) * kTileStep;
-    const int ksteps = nblk * KB / 16;
-    tc_mma_ts_lh(od, ps, vlo, md.hi, C::kIdescPV, first ? 0u : 1u);
+    // K = 16 keys per MMA: eight for a step of one 128-key block or two 64-key blocks, four
+    // for a lone 64-key block.  The second block's four go in under one branch (a branch
+    // between two MMAs slows their issue).
+    auto pv = [&](int kk) {
+      tc_mma_ts_lh(od, ps + kk * 8,
+                   vlo + ((((kk * 16) / KB) * C::kBlkB + ((kk * 16) % KB) * 128) >> 4), md.hi,
+                   C::kIdescPV, (kk == 0 && first) ? 0u : 1u);
+    };
+    static_assert(C::kKR == 128, "a step is 128 keys");
 #pragma unroll
-    for (int kk = 1; kk < C::kKR / 16; ++kk)
-      if (kk < ksteps)
-        tc_mma_ts_lh(od, ps + kk * 8,
-                     vlo + ((((kk * 16) / KB) * C::kBlkB + ((kk * 16) % KB) * 128) >> 4), md.hi,
-                     C::kIdescPV, 1u);
+    for (int kk = 0; kk < (KB == 128 ? 8 : 4); ++kk) pv(kk);
+    if (KB == 64 && nblk > 1) {
+#pragma unroll
+      for (int kk = 4; kk < 8; ++kk) pv(kk);
+    }
     tc_commit(bar(C::kBarPVD + g % 3));
   }
   tc_commit(bar(C::kBarDrainP));
