@@ -23,7 +23,8 @@
 //   warp 0      TMA producer: item tiles (one 3-D copy each) and step tiles; in dK/dV mode
 //               X and Y in two stages plus the step's lse and delta (bulk copies), in dQ
 //               mode X (= K) in a ring of three and Y (= V) in a ring of two.
-//   warp 1      MMA issuer (one thread) and TMEM owner.
+//   warp 1      MMA issuer (one thread) and TMEM owner; in dK/dV mode it issues MMA1 and
+//               MMA2, and a second issuing warp after the elementwise ones MMA3 and MMA4.
 //   warps 2..   elementwise warpgroups (two at b = 128, one at b = 64), laid out as the
 //               forward's softmax: per step they read T1 and T2, form P and dS, and write
 //               the bf16 operands for the second MMAs into TMEM.  At an item's end they
@@ -52,7 +53,9 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // elementwise warpgroups
   static constexpr int kEwWarps = 4 * kNumWG;
-  static constexpr int kThreads = 32 * (2 + kEwWarps);
+  // dK/dV mode: a second MMA-issuing warp after the elementwise ones (dV and dK products).
+  static constexpr int kMma2Warp = 2 + kEwWarps;
+  static constexpr int kThreads = 32 * (2 + kEwWarps + (KV ? 1 : 0));
   static constexpr int kG = 128 / BLK;           // column blocks per step
   static constexpr int kItemTile = BLK * D * 2;  // one item tile (A or B)
   static constexpr int kStepTile = 128 * D * 2;  // one step tile (X or Y), kG blocks
@@ -87,8 +90,10 @@ struct BwdCfg {
   static constexpr int kBarDL = 20;   // dK/dV mode: T2 loaded by every elementwise warp
   static constexpr int kBarIFV = 21;  // dK/dV mode: item tile B (V) landed; kBarIF is A's
   static constexpr int kBarIEV = 22;  // dK/dV mode: item tile B free; kBarIE is A's
-  static constexpr int kNumBars = 23;
-  static constexpr int kBarBytes = 192;  // barriers, TMEM slot, abort flag
+  static constexpr int kBarVI = 23;   // dK/dV mode: MMA3 (dV) of a step issued
+  static constexpr int kBarDrain2 = 24;
+  static constexpr int kNumBars = 25;
+  static constexpr int kBarBytes = 256;  // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -310,13 +315,12 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   if constexpr (KV) {
     // T1(t) (S^T, then E1 = P^T in its first 64 columns and E2 = dS^T in the next 64) is
     // the region at 0 on even steps and at 128 on odd ones; T2(t) (dP^T) is the other.
-    // Per step t:
+    // Two issuing threads: this one puts in MMA1 and MMA2 (both operands in shared
+    // memory), the other (bwd_mma_kv2) MMA3 and MMA4.  Per step t, here:
     //   MMA2(t) into T2(t) = T1(t-1), once MMA3/MMA4(t-1) have read E1/E2 there;
-    //   MMA3(t) (dV += P^T dO) once E1 is written;
-    //   MMA1(t+1) into T1(t+1) = T2(t), once every elementwise warp has loaded dP^T(t);
-    //   MMA4(t) (dK += dS^T Q) once E2 is written.
-    // So MMA3(t) and MMA1(t+1) run while the warps form dS^T(t), and MMA4(t) and
-    // MMA2(t+1) while they form P^T(t+1).
+    //   MMA1(t+1) into T1(t+1) = T2(t), once every elementwise warp has loaded dP^T(t)
+    //   and MMA3(t) has been issued (so that E1 of step t+1, which needs this MMA1,
+    //   cannot complete before the other thread has waited for E1 of step t).
     auto reg1 = [&](int t) { return tmem + ((t & 1) ? C::kT2 : C::kT1); };
     auto reg2 = [&](int t) { return tmem + ((t & 1) ? C::kT1 : C::kT2); };
     if (c.valid()) {
@@ -334,45 +338,26 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
         if (last) tc_commit(bar(C::kBarIE));
       }
       for (int t = 0; ok; ++t) {
-        const uint32_t st = (t % 2) * kStage;
         if (t > 0 && !mbar_wait(bar(C::kBarAD), (t - 1) & 1, ctl, kSiteMmaPvDone)) break;
         if (first && !mbar_wait(bar(C::kBarIFV), n & 1, ctl, kSiteMmaStage)) break;
         tc_fence_after();
-        issue_first(reg2(t), b0, y0 + st, nblk);  // dP^T = V dO^T
+        issue_first(reg2(t), b0, y0 + (t % 2) * kStage, nblk);  // dP^T = V dO^T
         tc_commit(bar(C::kBarDF));
         if (last) tc_commit(bar(C::kBarIEV));
-        // An item's first accumulation overwrites the accumulators: the previous item's
-        // must have been read out.
-        if (!mbar_wait(bar(C::kBarEF1), t & 1, ctl, kSiteMmaPFull)) break;
-        if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+        if (!c.valid()) break;
+        nblk = c.nblk();
+        first = c.s == 0;
+        last = c.s == c.nsteps - 1;
+        c.advance(p);
+        if (!mbar_wait(bar(C::kBarDL), t & 1, ctl, kSiteMmaPFull)) break;
+        if (!mbar_wait(bar(C::kBarVI), t & 1, ctl, kSiteMmaPFull)) break;
+        if (first && !mbar_wait(bar(C::kBarIF), (n + 1) & 1, ctl, kSiteMmaStage)) break;
+        if (!mbar_wait(bar(C::kBarXF + (t + 1) % 2), ((t + 1) / 2) & 1, ctl, kSiteMmaStage)) break;
         tc_fence_after();
-        issue_second(acc1, reg1(t), ym0 + st, nblk, first);  // dV += P^T dO
-        const bool more = c.valid();
-        int nblk2 = 0;
-        bool first2 = false, last2 = false;
-        if (more) {
-          nblk2 = c.nblk();
-          first2 = c.s == 0;
-          last2 = c.s == c.nsteps - 1;
-          c.advance(p);
-          if (!mbar_wait(bar(C::kBarDL), t & 1, ctl, kSiteMmaPFull)) break;
-          if (first2 && !mbar_wait(bar(C::kBarIF), (n + 1) & 1, ctl, kSiteMmaStage)) break;
-          if (!mbar_wait(bar(C::kBarXF + (t + 1) % 2), ((t + 1) / 2) & 1, ctl, kSiteMmaStage)) break;
-          tc_fence_after();
-          issue_first(reg1(t + 1), a0, x0 + ((t + 1) % 2) * kStage, nblk2);
-          tc_commit(bar(C::kBarTF));
-          if (last2) tc_commit(bar(C::kBarIE));
-        }
-        if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
-        tc_fence_after();
-        issue_second(acc2, reg1(t) + 64, xm0 + st, nblk, first);  // dK += dS^T Q
-        tc_commit(bar(C::kBarAD));
-        tc_commit(bar(C::kBarXE + t % 2));
-        if (!more) break;
-        if (first2) ++n;
-        nblk = nblk2;
-        first = first2;
-        last = last2;
+        issue_first(reg1(t + 1), a0, x0 + ((t + 1) % 2) * kStage, nblk);
+        tc_commit(bar(C::kBarTF));
+        if (last) tc_commit(bar(C::kBarIE));
+        if (first) ++n;
       }
     }
   } else {
@@ -430,6 +415,59 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   }
   tc_commit(bar(C::kBarDrain));
   mbar_drain_wait(bar(C::kBarDrain), 0);
+}
+
+// dK/dV mode, second issuing thread: per step t, MMA3(t) (dV += P^T dO) once E1 is written
+// and MMA4(t) (dK += dS^T Q) once E2 is; their completion frees T1(t) and the step's
+// tiles.  An item's first accumulation overwrites the accumulators, so it waits until
+// the previous item's have been read out.
+template <int BLK, int D>
+__device__ __forceinline__ void bwd_mma_kv2(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                            const WaitCtl& ctl) {
+  using C = BwdCfg<BLK, D, true>;
+  constexpr int G = C::kG;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const uint64_t x_desc = sdesc_sw128(sbase + C::kOffX, C::kHalf, 1024);
+  const uint32_t hi = static_cast<uint32_t>(x_desc >> 32);
+  const uint32_t xm0 = static_cast<uint32_t>(x_desc);
+  const uint32_t ym0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, C::kHalf, 1024));
+  constexpr uint32_t kStage = C::kStepTile >> 4;
+  const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
+  auto issue_second = [&](uint32_t acc, uint32_t te, uint32_t sm, int nblk, bool first) {
+    auto one = [&](int kk) {
+      const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+      tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
+    };
+#pragma unroll
+    for (int kk = 0; kk < (BLK == 128 ? 8 : 4); ++kk) one(kk);
+    if (BLK == 64 && nblk > 1) {
+#pragma unroll
+      for (int kk = 4; kk < 8; ++kk) one(kk);
+    }
+  };
+  StepCursor<G> c;
+  c.init(p);
+  int n = -1;
+  for (int t = 0; c.valid(); ++t) {
+    const int nblk = c.nblk();
+    const bool first = c.s == 0;
+    c.advance(p);
+    if (first) ++n;
+    const uint32_t t1 = tmem + ((t & 1) ? C::kT2 : C::kT1);
+    const uint32_t st = (t % 2) * kStage;
+    if (!mbar_wait(bar(C::kBarEF1), t & 1, ctl, kSiteMmaPFull)) break;
+    if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+    tc_fence_after();
+    issue_second(acc1, t1, ym0 + st, nblk, first);  // dV += P^T dO
+    mbar_arrive(bar(C::kBarVI));
+    if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
+    tc_fence_after();
+    issue_second(acc2, t1 + 64, xm0 + st, nblk, first);  // dK += dS^T Q
+    tc_commit(bar(C::kBarAD));
+    tc_commit(bar(C::kBarXE + t % 2));
+  }
+  tc_commit(bar(C::kBarDrain2));
+  mbar_drain_wait(bar(C::kBarDrain2), 0);
 }
 
 // ----------------------------------------------------------- elementwise warps
@@ -662,6 +700,9 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
     if (lane == 0) bwd_producer<BLK, D, KV>(p, &tm_a, &tm_b, &tm_x, &tm_y, sbase, ctl);
   } else if (warp == 1) {
     if (lane == 0) bwd_mma<BLK, D, KV>(p, sbase, tmem, ctl);
+  } else if (KV && warp == C::kMma2Warp) {
+    if constexpr (KV)
+      if (lane == 0) bwd_mma_kv2<BLK, D>(p, sbase, tmem, ctl);
   } else {
     bwd_elementwise<BLK, D, KV>(p, sbase, smem, tmem, ctl);
   }
