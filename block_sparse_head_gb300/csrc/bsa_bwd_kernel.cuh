@@ -23,8 +23,8 @@
 //   warp 0      TMA producer: item tiles (one 3-D copy each) and step tiles; in dK/dV mode
 //               X and Y in two stages plus the step's lse and delta (bulk copies), in dQ
 //               mode X (= K) in a ring of three and Y (= V) in a ring of two.
-//   warp 1      MMA issuer (one thread) and TMEM owner; in dK/dV mode it issues MMA1 and
-//               MMA2, and a second issuing warp after the elementwise ones MMA3 and MMA4.
+//   warp 1      MMA issuer (one thread) and TMEM owner: MMA1 and MMA2.  A second issuing
+//               warp after the elementwise ones issues MMA3 (and MMA4).
 //   warps 2..   elementwise warpgroups (two at b = 128, one at b = 64), laid out as the
 //               forward's softmax: per step they read T1 and T2, form P and dS, and write
 //               the bf16 operands for the second MMAs into TMEM.  At an item's end they
@@ -37,9 +37,10 @@
 // barrier of its own, so that A reloads once the item's last MMA1 is done.
 // dQ mode: T1 alternates between two 128-column regions (steps of even and odd index)
 // beside T2 and acc1.  MMA1 of step t goes in as soon as MMA3 of step t-2 has read its
-// region, so it runs while the elementwise warps work on step t-1; MMA3 of step t-1 goes in
-// after MMA2 of step t, so it runs while they work on step t.  An item's accumulator is
-// read out at the next item's first step, after that step's operands are handed over.
+// region, so it runs while the elementwise warps work on step t-1; MMA3 of step t-1, from
+// the second issuing thread, goes in once dS of step t-1 is written.  An item's
+// accumulator is read out at the next item's first step, after that step's operands are
+// handed over.
 // Every wait is bounded (WaitCtl), as in the forward.
 #pragma once
 
@@ -53,9 +54,10 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kNumWG = (BLK == 128) ? 2 : 1;  // elementwise warpgroups
   static constexpr int kEwWarps = 4 * kNumWG;
-  // dK/dV mode: a second MMA-issuing warp after the elementwise ones (dV and dK products).
+  // A second MMA-issuing warp after the elementwise ones (the products with an operand
+  // in TMEM: dQ, or dV and dK).
   static constexpr int kMma2Warp = 2 + kEwWarps;
-  static constexpr int kThreads = 32 * (2 + kEwWarps + (KV ? 1 : 0));
+  static constexpr int kThreads = 32 * (3 + kEwWarps);
   static constexpr int kG = 128 / BLK;           // column blocks per step
   static constexpr int kItemTile = BLK * D * 2;  // one item tile (A or B)
   static constexpr int kStepTile = 128 * D * 2;  // one step tile (X or Y), kG blocks
@@ -92,7 +94,8 @@ struct BwdCfg {
   static constexpr int kBarIEV = 22;  // dK/dV mode: item tile B free; kBarIE is A's
   static constexpr int kBarVI = 23;   // dK/dV mode: MMA3 (dV) of a step issued
   static constexpr int kBarDrain2 = 24;
-  static constexpr int kNumBars = 25;
+  static constexpr int kBarQI = 25;   // dQ mode: MMA3 (dQ) of a step issued
+  static constexpr int kNumBars = 26;
   static constexpr int kBarBytes = 256;  // barriers, TMEM slot, abort flag
   static_assert(kNumBars * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
@@ -255,20 +258,15 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
   constexpr int G = C::kG;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
   // Descriptor low words (start address >> 4 and the leading offset); the high word
-  // (stride 1024, version, 128-byte swizzle) is shared.  K-major for the first MMAs,
-  // MN-major (columns d contiguous, halves kHalf apart) for the step tiles as B of the
-  // second ones.
+  // (stride 1024, version, 128-byte swizzle) is shared.  K-major operands.
   const uint64_t a_desc = sdesc_sw128(sbase + C::kOffA, 16, 1024);
   const uint32_t hi = static_cast<uint32_t>(a_desc >> 32);
   const uint32_t a0 = static_cast<uint32_t>(a_desc);
   const uint32_t b0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffB, 16, 1024));
   const uint32_t x0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffX, 16, 1024));
   const uint32_t y0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, 16, 1024));
-  const uint32_t xm0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffX, C::kHalf, 1024));
-  const uint32_t ym0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, C::kHalf, 1024));
   constexpr uint32_t kStage = C::kStepTile >> 4;
   const uint32_t t2 = tmem + C::kT2;
-  const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
   // T = item tile (A or B) x step tile^T over d: one N = 128 MMA per 16 columns of d, or
   // one N = 64 MMA per block at b = 64.
   // A branch between two MMAs slows their issue, so the block count of a step is tested
@@ -294,21 +292,6 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
     else
       mmas(1);
   };
-  // acc += E (bf16 in TMEM, 128 columns of the step) x step tile (MN-major); K = 16 rows
-  // of the step per MMA.
-  auto issue_second = [&](uint32_t acc, uint32_t te, uint32_t sm, int nblk, bool first) {
-    auto one = [&](int kk) {
-      const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-      tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
-    };
-#pragma unroll
-    for (int kk = 0; kk < (BLK == 128 ? 8 : 4); ++kk) one(kk);
-    if (BLK == 64 && nblk > 1) {
-#pragma unroll
-      for (int kk = 4; kk < 8; ++kk) one(kk);
-    }
-  };
-
   StepCursor<G> c;
   c.init(p);
   int n = -1;
@@ -361,60 +344,93 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t sbase, uint
       }
     }
   } else {
-    // Step u's T1 region, and its accumulation once E1 (dS) is written: dQ += dS K.
+    // This thread issues MMA1 and MMA2; the other (bwd_mma_dq2) MMA3 (dQ += dS K).
     auto t1_of = [&](int u) { return tmem + ((u & 1) ? C::kT1b : C::kT1); };
-    auto mma3 = [&](int u, int nb, bool fst, int item) -> bool {
-      // An item's first accumulation overwrites acc1: the previous item's must have been
-      // read out.
-      if (fst && item > 0 && !mbar_wait(bar(C::kBarAR), (item - 1) & 1, ctl, kSiteMmaPFull))
-        return false;
-      tc_fence_after();
-      issue_second(acc1, t1_of(u), xm0 + (u % 3) * kStage, nb, fst);
-      tc_commit(bar(C::kBarAD + (u & 1)));
-      tc_commit(bar(C::kBarXE + u % 3));
-      return true;
-    };
-    int t = 0;
-    bool ok = true;
-    int pnb = 0, pitem = -1;  // step t-1: block count, item
-    bool pfirst = false;
-    for (; c.valid(); ++t) {
+    for (int t = 0; c.valid(); ++t) {
       const int nblk = c.nblk();
       const bool first = c.s == 0;
       const bool last = c.s == c.nsteps - 1;
       c.advance(p);
       if (first) {
         ++n;
-        if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+        if (!mbar_wait(bar(C::kBarIF), n & 1, ctl, kSiteMmaStage)) break;
       }
-      if (!mbar_wait(bar(C::kBarXF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+      if (!mbar_wait(bar(C::kBarXF + t % 3), (t / 3) & 1, ctl, kSiteMmaStage)) break;
       // This T1 region held step t-2, whose MMA3 read E1 from it (AD of that region cannot
       // be a phase ahead: its next phase is step t's own MMA3).
-      if (t >= 2 && !mbar_wait(bar(C::kBarAD + (t & 1)), ((t - 2) / 2) & 1, ctl, kSiteMmaPvDone)) {
-        ok = false;
+      if (t >= 2 && !mbar_wait(bar(C::kBarAD + (t & 1)), ((t - 2) / 2) & 1, ctl, kSiteMmaPvDone))
         break;
-      }
       tc_fence_after();
       issue_first(t1_of(t), a0, x0 + (t % 3) * kStage, nblk);  // S = Q K^T
-      // T2 is free, and E1 of step t-1 written, once the elementwise warps finished it.
-      if (t >= 1 && !mbar_wait(bar(C::kBarEF), (t - 1) & 1, ctl, kSiteMmaPFull)) { ok = false; break; }
-      if (!mbar_wait(bar(C::kBarYF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) { ok = false; break; }
+      // T2 is free once the elementwise warps finished step t-1.
+      if (t >= 1 && !mbar_wait(bar(C::kBarEF), (t - 1) & 1, ctl, kSiteMmaPFull)) break;
+      if (!mbar_wait(bar(C::kBarYF + t % 2), (t / 2) & 1, ctl, kSiteMmaStage)) break;
       tc_fence_after();
       issue_first(t2, b0, y0 + (t % 2) * kStage, nblk);  // dP = dO V^T
       tc_commit(bar(C::kBarTF));
       tc_commit(bar(C::kBarYE + t % 2));
       if (last) tc_commit(bar(C::kBarIE));
-      if (t >= 1 && !mma3(t - 1, pnb, pfirst, pitem)) { ok = false; break; }
-      pnb = nblk;
-      pfirst = first;
-      pitem = n;
-    }
-    if (ok && t >= 1) {
-      if (mbar_wait(bar(C::kBarEF), (t - 1) & 1, ctl, kSiteMmaPFull)) mma3(t - 1, pnb, pfirst, pitem);
     }
   }
   tc_commit(bar(C::kBarDrain));
   mbar_drain_wait(bar(C::kBarDrain), 0);
+}
+
+// acc += E (bf16 in TMEM, 128 columns of the step) x step tile (MN-major: columns d
+// contiguous, halves kHalf apart); K = 16 rows of the step per MMA.  A branch between two
+// MMAs slows their issue, so the block count is tested once.
+template <int BLK, int D, bool KV>
+__device__ __forceinline__ void bwd_issue_second(uint32_t acc, uint32_t te, uint32_t sm,
+                                                 uint32_t hi, int nblk, bool first) {
+  using C = BwdCfg<BLK, D, KV>;
+  auto one = [&](int kk) {
+    const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
+    tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
+  };
+#pragma unroll
+  for (int kk = 0; kk < (BLK == 128 ? 8 : 4); ++kk) one(kk);
+  if (BLK == 64 && nblk > 1) {
+#pragma unroll
+    for (int kk = 4; kk < 8; ++kk) one(kk);
+  }
+}
+
+// dQ mode, second issuing thread: per step u, MMA3(u) (dQ += dS K, dS over T1 of step u)
+// once the warps have written dS; its completion frees that T1 region and the step's K
+// slot.  Each MMA3 issued is marked on a barrier that the warps wait for before they hand
+// over the next step's dS, so this thread cannot fall two phases behind the dS barrier.
+template <int BLK, int D>
+__device__ __forceinline__ void bwd_mma_dq2(const BwdParams& p, uint32_t sbase, uint32_t tmem,
+                                            const WaitCtl& ctl) {
+  using C = BwdCfg<BLK, D, false>;
+  constexpr int G = C::kG;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8 * i; };
+  const uint64_t x_desc = sdesc_sw128(sbase + C::kOffX, C::kHalf, 1024);
+  const uint32_t hi = static_cast<uint32_t>(x_desc >> 32);
+  const uint32_t xm0 = static_cast<uint32_t>(x_desc);
+  constexpr uint32_t kStage = C::kStepTile >> 4;
+  const uint32_t acc1 = tmem + C::kAcc1;
+  StepCursor<G> c;
+  c.init(p);
+  int n = -1;
+  for (int u = 0; c.valid(); ++u) {
+    const int nblk = c.nblk();
+    const bool first = c.s == 0;
+    c.advance(p);
+    if (first) ++n;
+    if (!mbar_wait(bar(C::kBarEF), u & 1, ctl, kSiteMmaPFull)) break;
+    // An item's first accumulation overwrites acc1: the previous item's must have been
+    // read out.
+    if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
+    tc_fence_after();
+    bwd_issue_second<BLK, D, false>(acc1, tmem + ((u & 1) ? C::kT1b : C::kT1),
+                                    xm0 + (u % 3) * kStage, hi, nblk, first);
+    tc_commit(bar(C::kBarAD + (u & 1)));
+    tc_commit(bar(C::kBarXE + u % 3));
+    mbar_arrive(bar(C::kBarQI));
+  }
+  tc_commit(bar(C::kBarDrain2));
+  mbar_drain_wait(bar(C::kBarDrain2), 0);
 }
 
 // dK/dV mode, second issuing thread: per step t, MMA3(t) (dV += P^T dO) once E1 is written
@@ -433,18 +449,6 @@ __device__ __forceinline__ void bwd_mma_kv2(const BwdParams& p, uint32_t sbase, 
   const uint32_t ym0 = static_cast<uint32_t>(sdesc_sw128(sbase + C::kOffY, C::kHalf, 1024));
   constexpr uint32_t kStage = C::kStepTile >> 4;
   const uint32_t acc1 = tmem + C::kAcc1, acc2 = tmem + C::kAcc2;
-  auto issue_second = [&](uint32_t acc, uint32_t te, uint32_t sm, int nblk, bool first) {
-    auto one = [&](int kk) {
-      const uint32_t bo = ((((kk * 16) / BLK) * C::kBlkB + ((kk * 16) % BLK) * 128) >> 4);
-      tc_mma_ts_lh(acc, te + kk * 8, sm + bo, hi, C::kIdesc3, (first && kk == 0) ? 0u : 1u);
-    };
-#pragma unroll
-    for (int kk = 0; kk < (BLK == 128 ? 8 : 4); ++kk) one(kk);
-    if (BLK == 64 && nblk > 1) {
-#pragma unroll
-      for (int kk = 4; kk < 8; ++kk) one(kk);
-    }
-  };
   StepCursor<G> c;
   c.init(p);
   int n = -1;
@@ -458,11 +462,11 @@ __device__ __forceinline__ void bwd_mma_kv2(const BwdParams& p, uint32_t sbase, 
     if (!mbar_wait(bar(C::kBarEF1), t & 1, ctl, kSiteMmaPFull)) break;
     if (first && n > 0 && !mbar_wait(bar(C::kBarAR), (n - 1) & 1, ctl, kSiteMmaPFull)) break;
     tc_fence_after();
-    issue_second(acc1, t1, ym0 + st, nblk, first);  // dV += P^T dO
+    bwd_issue_second<BLK, D, true>(acc1, t1, ym0 + st, hi, nblk, first);  // dV += P^T dO
     mbar_arrive(bar(C::kBarVI));
     if (!mbar_wait(bar(C::kBarEF), t & 1, ctl, kSiteMmaPFull)) break;
     tc_fence_after();
-    issue_second(acc2, t1 + 64, xm0 + st, nblk, first);  // dK += dS^T Q
+    bwd_issue_second<BLK, D, true>(acc2, t1 + 64, xm0 + st, hi, nblk, first);  // dK += dS^T Q
     tc_commit(bar(C::kBarAD));
     tc_commit(bar(C::kBarXE + t % 2));
   }
@@ -629,6 +633,11 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, uint32_t sba
         }
         tmem_st_16x32bx2_x32<32>(t1, pk1);
         tmem_st_wait();
+        // The previous step's dQ product issued (see bwd_mma_dq2).
+        if (g >= 1 && !wait_bar(C::kBarQI, (g - 1) & 1, kSiteSoftSFull)) {
+          ok = false;
+          break;
+        }
         warp_arrive(C::kBarEF);
         if (s == 0 && pending && !read_pending()) {
           ok = false;
@@ -700,9 +709,13 @@ __global__ void __launch_bounds__(BwdCfg<BLK, D, KV>::kThreads, 1)
     if (lane == 0) bwd_producer<BLK, D, KV>(p, &tm_a, &tm_b, &tm_x, &tm_y, sbase, ctl);
   } else if (warp == 1) {
     if (lane == 0) bwd_mma<BLK, D, KV>(p, sbase, tmem, ctl);
-  } else if (KV && warp == C::kMma2Warp) {
-    if constexpr (KV)
-      if (lane == 0) bwd_mma_kv2<BLK, D>(p, sbase, tmem, ctl);
+  } else if (warp == C::kMma2Warp) {
+    if (lane == 0) {
+      if constexpr (KV)
+        bwd_mma_kv2<BLK, D>(p, sbase, tmem, ctl);
+      else
+        bwd_mma_dq2<BLK, D>(p, sbase, tmem, ctl);
+    }
   } else {
     bwd_elementwise<BLK, D, KV>(p, sbase, smem, tmem, ctl);
   }
