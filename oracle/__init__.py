@@ -6,6 +6,7 @@ from .bsa_oracle import (  # noqa: F401
     active_keys,
     backward,
     backward_blocks,
+    backward_sampled,
     block_flops,
     check_layout,
     expand_mask,

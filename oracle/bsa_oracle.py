@@ -341,6 +341,62 @@ def backward_blocks(q, k, v, do, layout, scale: float, block: int, causal_diag: 
     return dq, dk, dv
 
 
+def backward_sampled(q_bh, k_bh, v_bh, do_bh, layout_h, scale: float, block: int,
+                     causal_diag: bool, query_blocks, key_blocks):
+    """Chosen rows of ``backward_blocks``'s result for one (batch, head): dq of the query
+    blocks in ``query_blocks`` and dk, dv of the key blocks in ``key_blocks``, without the
+    rest of the work (the full-size workloads are too large for ``backward_blocks``).
+
+    Same source as ``backward``.  dq of query block i needs only the keys of its own
+    layout row; dk and dv of key block j are sums of one term per query block i whose
+    layout row lists j.  Each query block's P and dS over its active keys are formed as
+    in ``backward_blocks``.  Pinned against ``backward_blocks`` in
+    ``tests/test_oracle_bwd.py``.  Returns three dicts {block index: [block, d] array}."""
+    lay = check_layout(np.asarray(layout_h)[None])[0]
+    q = np.asarray(q_bh, dtype=np.float64)
+    k = np.asarray(k_bh, dtype=np.float64)
+    v = np.asarray(v_bh, dtype=np.float64)
+    do = np.asarray(do_bh, dtype=np.float64)
+    nb = lay.shape[0]
+    d = q.shape[1]
+    done = {}
+
+    def p_ds(i):  # (rows, cols, P, dS) of query block i, or None for an empty row
+        if i not in done:
+            active = [j for j in range(nb) if lay[i, j] == 1]
+            if not active:
+                done[i] = None
+            else:
+                rows = np.arange(i * block, (i + 1) * block)
+                cols = np.concatenate([np.arange(j * block, (j + 1) * block) for j in active])
+                mask = np.ones((block, cols.size), dtype=bool)
+                if causal_diag:
+                    mask &= ~((cols[None, :] // block == i) & (cols[None, :] > rows[:, None]))
+                s = np.where(mask, scale * (q[rows] @ k[cols].T), -np.inf)
+                e = np.exp(s - s.max(axis=1, keepdims=True))
+                p = e / e.sum(axis=1, keepdims=True)
+                dp = do[rows] @ v[cols].T
+                ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+                done[i] = (rows, cols, p, ds)
+        return done[i]
+
+    dq, dk, dv = {}, {}, {}
+    for i in query_blocks:
+        r = p_ds(i)
+        dq[i] = np.zeros((block, d)) if r is None else scale * (r[3] @ k[r[1]])
+    for j in key_blocks:
+        gk, gv = np.zeros((block, d)), np.zeros((block, d))
+        for i in range(nb):
+            if lay[i, j] != 1:
+                continue
+            rows, cols, p, ds = p_ds(i)
+            sel = cols // block == j
+            gk += scale * (ds[:, sel].T @ q[rows])
+            gv += p[:, sel].T @ do[rows]
+        dk[j], dv[j] = gk, gv
+    return dq, dk, dv
+
+
 def oracle_csc(layout, batch: int):
     """Column view of the layout for the key-side gradients: for each (h, j) the active
     query blocks i ascending (col_ptr [H*nb+1], row_idx [nnz]) and one item

@@ -104,3 +104,50 @@ def test_negative_and_zero_scale():
         ref = oracle.backward(*(t.double().numpy() for t in (q, k, v, do)), lay.numpy(), scale,
                               block, True)
         _compare(got, ref)
+
+
+@pytest.mark.parametrize("index", [4, 5])
+def test_workload_full_size_sampled(index, parity_report):
+    """Full-size backward in the benchmark's configuration: every gradient finite, and the
+    rows of three (batch, head) pairs compared with the fp64 oracle -- dq of the longest
+    and of random query blocks, dk and dv of the most attended, of random and (if any)
+    of unattended key blocks."""
+    wl = wls.WORKLOADS[index]
+    q, k, v = wls.qkv(wl)
+    do = wls.randn_qkv(wl.B, wl.H, wl.L, wl.d, seed=5000 + index)[0]
+    lay = wls.layout_for(wl)
+    lut = bsa.build_lut(lay, wl.B)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = bsa.forward(qd, kd, vd, lut, wl.scale, wl.block, wl.causal_diag)
+    g = bsa.backward(qd, kd, vd, o, lse, dod, lut, wl.scale, wl.block, wl.causal_diag)
+    st, word = lut.device_status()
+    assert st == 0, hex(word)
+    for t, what in zip(g, ("dq", "dk", "dv")):
+        assert bool(torch.isfinite(t).all()), what
+    dq, dk, dv = (t.float().cpu().numpy() for t in g)
+    del qd, kd, vd, dod, o, lse, g
+    lay_np = lay.numpy()
+    nb, blk = lay_np.shape[1], wl.block
+    rng = np.random.default_rng(77 + index)
+    got, ref = [[], [], []], [[], [], []]
+    for b, h in [(0, 0), (wl.B // 2, wl.H // 2), (wl.B - 1, wl.H - 1)]:
+        lh = lay_np[h]
+        rows, cols = lh.sum(axis=1), lh.sum(axis=0)
+        qb = sorted(set(np.argsort(-rows, kind="stable")[:3].tolist() +
+                        rng.choice(nb, 5, replace=False).tolist()))
+        kb = set(np.argsort(-cols, kind="stable")[:1].tolist() + rng.choice(nb, 6, replace=False).tolist())
+        if (cols == 0).any():
+            kb.add(int(np.flatnonzero(cols == 0)[0]))
+        kb = sorted(kb)
+        gq, gk, gv = oracle.backward_sampled(*(t[b, h].double().numpy() for t in (q, k, v, do)), lh,
+                                             wl.scale, blk, wl.causal_diag, qb, kb)
+        for i in qb:
+            got[0].append(dq[b, h, i * blk:(i + 1) * blk])
+            ref[0].append(gq[i])
+        for j in kb:
+            got[1].append(dk[b, h, j * blk:(j + 1) * blk])
+            ref[1].append(gk[j])
+            got[2].append(dv[b, h, j * blk:(j + 1) * blk])
+            ref[2].append(gv[j])
+    _compare([np.stack(x) for x in got], [np.stack(x) for x in ref], parity_report,
+             f"{wl.name} (full size, sampled rows of 3 heads)")

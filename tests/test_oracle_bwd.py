@@ -192,3 +192,44 @@ def test_block_restricted_equals_dense():
         a = oracle.backward(q, k, v, do, lay, 0.4, blk, causal)
         b = oracle.backward_blocks(q, k, v, do, lay, 0.4, blk, causal)
         assert _err(a, b) < 1e-12
+
+
+def test_sampled_rows_equal_block_backward():
+    """``backward_sampled`` returns exactly the chosen rows of ``backward_blocks``: dq of
+    any query block, dk and dv of any key block (attended by many rows, by one, or by
+    none), with and without the causal diagonal."""
+    for seed, causal, blk in [(51, True, 4), (52, False, 3), (53, True, 5)]:
+        B, H, nb, d = 2, 2, 6, 5
+        L = nb * blk
+        q, k, v, do = (_rand((B, H, L, d), seed * 10 + s) for s in range(4))
+        lay = wls.random_layout(H, nb, 0.45, seed, empty_rows=1).numpy()
+        lay[0, :, 1] = 1  # a column every row attends
+        lay[1, :, 4] = 0  # a column no row attends
+        full = oracle.backward_blocks(q, k, v, do, lay, 0.3, blk, causal)
+        for b in range(B):
+            for h in range(H):
+                qb, kb = [0, 2, 5, 3], [1, 4, 0, 5]
+                dq, dk, dv = oracle.backward_sampled(q[b, h], k[b, h], v[b, h], do[b, h], lay[h],
+                                                     0.3, blk, causal, qb, kb)
+                for i in qb:
+                    assert np.abs(dq[i] - full[0][b, h, i * blk:(i + 1) * blk]).max() < 1e-12
+                for j in kb:
+                    assert np.abs(dk[j] - full[1][b, h, j * blk:(j + 1) * blk]).max() < 1e-12
+                    assert np.abs(dv[j] - full[2][b, h, j * blk:(j + 1) * blk]).max() < 1e-12
+                if h == 1:
+                    assert not dk[4].any() and not dv[4].any()
+
+
+def test_sampled_rows_planted_slip_fails():
+    """A sampled backward that drops the delta term of dS disagrees with the pinned one."""
+    blk, nb, d = 4, 5, 6
+    L = nb * blk
+    q, k, v, do = (_rand((L, d), 60 + s) for s in range(4))
+    lay = np.tril(np.ones((nb, nb), np.int64))
+    dq, dk, dv = oracle.backward_sampled(q, k, v, do, lay, 0.5, blk, True, [3], [1])
+    s = 0.5 * (q[12:16] @ k[:16].T)
+    s = np.where(np.arange(16)[None, :] > np.arange(12, 16)[:, None], -np.inf, s)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    ds_wrong = p * (do[12:16] @ v[:16].T)  # no "- delta"
+    assert np.abs(0.5 * ds_wrong @ k[:16] - dq[3]).max() > 1e-3
