@@ -376,8 +376,11 @@ int bsa_set_wait_limit(bsa_lut* lut, uint64_t ns);
  * 11 softmax, O free for a rescale; 12 the item's last PV done (forward: epilogue at
  * block 128, softmax at block 64; backward: softmax); 13 epilogue, the rows'
  * statistics written; 14 softmax, the previous rows' statistics read (sites 10, 13
- * and 14: the forward at block 128 only).  Errors: BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (site outside
- * [0, 65535]).
+ * and 14: the forward at block 128 only).  The backward's kernels use the same ids for
+ * their counterparts: 1 and 2 the producer's item and step slots free, 6 tiles landed,
+ * 7 the elementwise warps' operands written (or the accumulators read out), 8 a TMEM
+ * region free, 9 the elementwise warps waiting for a product, 12 an item's last
+ * products done.  Errors: BSA_ERR_NULL, BSA_ERR_UNSUPPORTED (site outside [0, 65535]).
  */
 int bsa_debug_expire_wait(bsa_lut* lut, int site);
 
